@@ -1,0 +1,503 @@
+"""Benchmark of the grouped quantize + grouped GEMM hot path.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxg|reference]
+                    [--config mixtral_fprop_mxfp8|finegrained_fprop_mxfp8|wgrad_mxfp8|
+                              rowscaled_fprop_nvfp4|tiny_fprop_mxfp8] [--out bf16|f32]
+
+One step is one pass of the whole path over one batch of synthetic input:
+  fprop:  group offsets -> quantize X (MXFP8 rowwise + transposed colwise, or
+          row-scaled NVFP4) -> quantize W (rowwise) -> grouped GEMM fprop
+  wgrad:  group offsets -> quantize X and dY (MXFP8 colwise, transposed) ->
+          grouped GEMM wgrad
+The metric is grouped quant+GEMM TFLOP/s: 2*M*N*K algorithmic FLOP of the
+GEMM over the time of the whole step, with the inputs resident in HBM.  Each
+step is timed with CUDA events on the launching stream; L2 is flushed (a
+512 MB write) before every timed step, outside its events.  "e2e" repeats the
+measurement through the same C-ABI calls with the inputs copied from pinned
+host memory and the output copied back inside the timed region.
+
+For N > 1 (torchrun) every rank runs an independent replica on its own GPU
+and its own seeded batch (the path has no exchange step); the job value is the
+FLOP of all ranks over the slowest rank's time.  ``--impl reference`` times
+the CPU oracle (the only other implementation there is) on a bounded sample
+of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped quant+GEMM TFLOP/s (frac of dense MXFP8 peak); quantize HBM GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- the path
+class Path:
+    """Device buffers and the C-ABI calls of one step."""
+
+    def __init__(self, wl, out_bf16: bool, dev, seed_offset: int = 0):
+        import torch
+        from moe_grouped_block_gb300 import mxg, workloads
+        self.mxg, self.torch = mxg, torch
+        self.wl = wl
+        self.dev = dev
+        if seed_offset:
+            wl = wl.scaled(seed=wl.seed + 1000 * seed_offset)
+        inp = workloads.make_inputs(wl)
+        self.host = inp
+        G, N, K, R = wl.G, wl.N, wl.K, wl.rows_capacity
+        self.G, self.N, self.K, self.R = G, N, K, R
+        self.sizes = inp["sizes"].to(dev)
+        self.x = inp["x"].to(dev)
+        self.ws = mxg.alloc_offsets(G, dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out_type = mxg.MXG_OUT_BF16 if out_bf16 else mxg.MXG_OUT_F32
+        cdt = torch.bfloat16 if out_bf16 else torch.float32
+        if wl.mode == "fprop":
+            self.w = inp["w"].to(dev).reshape(G * N, K)
+            if wl.fmt == "mxfp8":
+                self.qx = mxg.alloc_mxfp8(R, K, rowwise=True, colwise=True, device=dev)
+                self.qw = mxg.alloc_mxfp8(G * N, K, device=dev)
+            else:
+                self.qx = mxg.alloc_nvfp4(R, K, device=dev)
+                self.qw = mxg.alloc_nvfp4(G * N, K, device=dev)
+            self.C = torch.empty((R, N), dtype=cdt, device=dev)
+        else:
+            self.dy = inp["dy"].to(dev)
+            self.qx = mxg.alloc_mxfp8(R, K, rowwise=False, colwise=True, device=dev)
+            self.qd = mxg.alloc_mxfp8(R, N, rowwise=False, colwise=True, device=dev)
+            self.C = torch.empty((G, N, K), dtype=cdt, device=dev)
+
+    # each stage returns nothing; all work is enqueued on the current stream
+    def stages(self):
+        m, wl = self.mxg, self.wl
+        G, N, K, R = self.G, self.N, self.K, self.R
+        out = []
+        out.append(("group_offsets", lambda: m.mxg_group_offsets(self.sizes, 1, K, R, self.ws,
+                                                                 self.status)))
+        if wl.mode == "fprop" and wl.fmt == "mxfp8":
+            q = self.qx
+            out.append(("quantize_x_mxfp8_both", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_BOTH, self.x, R, K, self.ws, G, q["q_row"], q["sf_row"],
+                q["q_col"], q["sf_col"], None, self.status)))
+            out.append(("quantize_w_mxfp8_row", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_ROWWISE, self.w, G * N, K, None, G, self.qw["q_row"],
+                self.qw["sf_row"], None, None, None, self.status)))
+            out.append(("grouped_gemm_fprop_mxfp8", lambda: m.mxg_grouped_gemm(
+                m.MXG_MXFP8_E4M3, m.MXG_FPROP_TN, (q["q_row"], q["sf_row"], None),
+                (self.qw["q_row"], self.qw["sf_row"], None), self.ws, G, R, N, K, C=self.C,
+                out_type=self.out_type, dev_status=self.status)))
+        elif wl.mode == "fprop":
+            q, qw = self.qx, self.qw
+            out.append(("quantize_x_nvfp4", lambda: m.mxg_group_quantize(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_ROWWISE, self.x, R, K, self.ws, G, q["q_row"],
+                q["sf_row"], None, None, q["outer_row"], self.status)))
+            out.append(("quantize_w_nvfp4", lambda: m.mxg_group_quantize(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_ROWWISE, self.w, G * N, K, None, G, qw["q_row"],
+                qw["sf_row"], None, None, qw["outer_row"], self.status)))
+            out.append(("grouped_gemm_fprop_nvfp4", lambda: m.mxg_grouped_gemm(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_FPROP_TN, (q["q_row"], q["sf_row"], q["outer_row"]),
+                (qw["q_row"], qw["sf_row"], qw["outer_row"]), self.ws, G, R, N, K, C=self.C,
+                out_type=self.out_type, dev_status=self.status)))
+        else:
+            out.append(("quantize_x_mxfp8_col", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_COLWISE, self.x, R, K, self.ws, G, None, None,
+                self.qx["q_col"], self.qx["sf_col"], None, self.status)))
+            out.append(("quantize_dy_mxfp8_col", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_COLWISE, self.dy, R, N, self.ws, G, None, None,
+                self.qd["q_col"], self.qd["sf_col"], None, self.status)))
+            out.append(("grouped_gemm_wgrad_mxfp8", lambda: m.mxg_grouped_gemm(
+                m.MXG_MXFP8_E4M3, m.MXG_WGRAD_NT, (self.qd["q_col"], self.qd["sf_col"], None),
+                (self.qx["q_col"], self.qx["sf_col"], None), self.ws, G, R, N, K, C=self.C,
+                out_type=self.out_type, dev_status=self.status)))
+        return out
+
+    def kernel_bytes(self, name: str) -> float:
+        """Algorithmic HBM bytes of one launch (inputs read once, outputs
+        written once; the GEMM's are reported too though it is tensor-bound)."""
+        wl, G, N, K, R = self.wl, self.G, self.N, self.K, self.R
+        M = wl.M
+        obytes = self.C.element_size()
+        if name == "group_offsets":
+            return 4 * G + 8 * (2 * G + 1)
+        if name == "quantize_x_mxfp8_both":
+            return M * K * (2 + 2 + 2 / 32)
+        if name == "quantize_w_mxfp8_row":
+            return G * N * K * (2 + 1 + 1 / 32)
+        if name == "quantize_x_nvfp4":
+            return M * K * (2 + 0.5 + 1 / 16) + 4 * M
+        if name == "quantize_w_nvfp4":
+            return G * N * K * (2 + 0.5 + 1 / 16) + 4 * G * N
+        if name == "quantize_x_mxfp8_col":
+            return M * K * (2 + 1 + 1 / 32)
+        if name == "quantize_dy_mxfp8_col":
+            return M * N * (2 + 1 + 1 / 32)
+        sizes = self.host["sizes"].numpy()
+        live_experts = int((sizes > 0).sum())
+        if name == "grouped_gemm_fprop_mxfp8":
+            return M * K * (1 + 1 / 32) + live_experts * N * K * (1 + 1 / 32) + M * N * obytes
+        if name == "grouped_gemm_fprop_nvfp4":
+            return (M * K * (0.5 + 1 / 16) + live_experts * N * K * (0.5 + 1 / 16) + M * N * obytes
+                    + 4 * (M + live_experts * N))
+        if name == "grouped_gemm_wgrad_mxfp8":
+            return (N + K) * M * (1 + 1 / 32) + G * N * K * obytes
+        return 0.0
+
+    def input_tensors(self):
+        if self.wl.mode == "fprop":
+            return [("sizes", self.sizes), ("x", self.x), ("w", self.w)]
+        return [("sizes", self.sizes), ("x", self.x), ("dy", self.dy)]
+
+
+def run_mxg(args, wl, ws_world, rank, local):
+    import torch
+    from moe_grouped_block_gb300 import mxg
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if ws_world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    path = Path(wl, args.out == "bf16", dev, seed_offset=rank)
+    stages = path.stages()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        for _, fn in stages:
+            fn()
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if int(path.status.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(path.status.item()))
+
+    # ---- timed region: K steps, per-step and per-kernel CUDA events
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in stages] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = mxg.mxg_launch_count()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(1.0)
+        for (name, fn), (e0, e1) in zip(stages, ev[s]):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    launches = mxg.mxg_launch_count() - launches0
+    clk = clocks.stop()
+    per_kernel = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+                  for i, (name, _) in enumerate(stages)}
+    step_ms = [ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]
+    ms = float(np.mean(step_ms))
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(path.status.item()) != 0:
+        raise RuntimeError("device status %d" % int(path.status.item()))
+
+    # ---- e2e: host buffers, copies inside the timed region
+    host_in = [(n, t.cpu().pin_memory()) for n, t in path.input_tensors()]
+    host_out = torch.empty(path.C.shape, dtype=path.C.dtype).pin_memory()
+    dev_in = dict(path.input_tensors())
+    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n, t in host_in:
+            dev_in[n].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(path.C, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    for e0, e1 in e2e_ev:
+        flush.fill_(1.0)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks, peak_src = load_peaks()
+    flops = wl.flops()
+    kernels = {}
+    for name, times in per_kernel.items():
+        t = float(np.mean(times))
+        d = {"ms": round(t, 5)}
+        b = path.kernel_bytes(name)
+        if b:
+            d["GB/s"] = round(b / (t * 1e-3) / 1e9, 1)
+            d["hbm_frac"] = round(b / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+        if name.startswith("grouped_gemm"):
+            d["TFLOP/s"] = round(flops / (t * 1e-3) / 1e12, 1)
+        kernels[name] = d
+    gemm_name = [n for n in per_kernel if n.startswith("grouped_gemm")][0]
+    gemm_ms = float(np.mean(per_kernel[gemm_name]))
+    nvfp4 = wl.fmt == "nvfp4"
+    # dense MXFP8 peak = measured bf16 peak x 2 (nominal fp8 : bf16 ratio);
+    # NVFP4 x 6 (nominal 13.5 : 2.25)
+    peak_tc = peaks["bf16_tflops"] * (6.0 if nvfp4 else 2.0)
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": gemm_name, "achieved": round(achieved, 1),
+                "peak": round(peak_tc, 1), "unit": "TFLOP/s", "frac": round(achieved / peak_tc, 4),
+                "peak_source": "%s bf16_tflops (burst) x %d" % (peak_src, 6 if nvfp4 else 2),
+                "traffic": None}
+    if nvfp4:  # the NVFP4 layer is HBM-bound: report the time roofline too
+        b = path.kernel_bytes(gemm_name)
+        roofline["hbm_bytes"] = b
+        roofline["t_hbm_roofline_ms"] = round(b / (peaks["hbm_gbs"] * 1e9) * 1e3, 5)
+    value = ws_world * flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4(e2m1/ue4m3)->f32" if nvfp4 else "mxfp8(e4m3/e8m0)->f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": wl.name, "G": wl.G, "K": wl.K, "N": wl.N, "M": wl.M,
+                   "mode": wl.mode, "out": args.out,
+                   "step": " -> ".join(n for n, _ in stages),
+                   "l2": "flushed before every timed step (512 MB write); inputs also exceed L2",
+                   "parallelism": "replicas" if ws_world > 1 else "single GPU"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": {"value": round(ws_world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def _oracle_sample(wl, rows_per_group: int, cols_per_group: int):
+    """One bounded sample of the workload through the oracle: quantize the
+    sampled activation rows and weight rows, then the fp64 GEMM on them.
+    Returns (seconds, algorithmic GEMM FLOP of the sample)."""
+    import torch
+    import oracle
+    from moe_grouped_block_gb300 import workloads
+    inp = workloads.make_inputs(wl) if not hasattr(wl, "_cached") else wl._cached
+    sizes = inp["sizes"].numpy()
+    G, N, K = wl.G, wl.N, wl.K
+    flop = 0.0
+    t0 = time.perf_counter()
+    ws, _ = oracle.group_offsets(sizes, 1, K, wl.rows_capacity)
+    offs = oracle.live_rows(ws, G)
+    for g in range(G):
+        lo, hi = int(offs[g]), int(offs[g + 1])
+        if hi == lo:
+            continue
+        r = min(rows_per_group, hi - lo)
+        r128 = max(128, (r + 127) // 128 * 128)
+        lo2 = min(lo, hi - r128) if hi - lo >= r128 else lo
+        c128 = max(128, min(N, (cols_per_group + 127) // 128 * 128))
+        if wl.mode == "fprop":
+            xs = inp["x"][lo2:lo2 + r128]
+            wsub = inp["w"][g, :c128]
+            if wl.fmt == "mxfp8":
+                qa = oracle.mxfp8_quantize(xs, r128, r128, rowwise=True, colwise=True)
+                qb = oracle.mxfp8_quantize(wsub, c128, c128)
+                a = {"q": qa["q_row"], "sf": qa["sf_row"]}
+                b = {"q": qb["q_row"], "sf": qb["sf_row"]}
+            else:
+                qa = oracle.nvfp4_quantize(xs, r128, r128)
+                qb = oracle.nvfp4_quantize(wsub, c128, c128)
+                a = {"q": qa["q_row"], "sf": qa["sf_row"], "outer": qa["outer_row"]}
+                b = {"q": qb["q_row"], "sf": qb["sf_row"], "outer": qb["outer_row"]}
+            oracle.grouped_gemm_fprop(wl.fmt, a, b, [0, r128], c128, K)
+            flop += 2.0 * r128 * c128 * K
+        else:
+            xs = inp["x"][lo2:lo2 + r128]
+            ds = inp["dy"][lo2:lo2 + r128, :c128].contiguous()
+            qx = oracle.mxfp8_quantize(xs, r128, r128, rowwise=False, colwise=True)
+            qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=False, colwise=True)
+            kk = min(K, c128)
+            oracle.grouped_gemm_wgrad({"q": qd["q_col"], "sf": qd["sf_col"]},
+                                      {"q": qx["q_col"], "sf": qx["sf_col"]}, [0, r128], r128,
+                                      c128, K, sample_k=np.arange(kk))
+            flop += 2.0 * r128 * c128 * kk
+    return time.perf_counter() - t0, flop
+
+
+def cpu_baseline(wl, budget_s: float = 15.0):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count()
+    # calibrate on a small sample, then size the sample to about budget_s
+    t_small, f_small = _oracle_sample(wl, 128, 128)
+    scale = max(1.0, min(64.0, budget_s / max(t_small, 1e-3)))
+    side = int(128 * np.sqrt(scale))
+    t, f = _oracle_sample(wl, side, side)
+    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": round(t, 2),
+            "sample": "per expert: %d activation rows x %d weight rows, full K=%d, quantize + "
+                      "fp64 GEMM (fprop) / colwise quantize + fp64 GEMM (wgrad)" % (
+                          min(side, wl.M), side, wl.K)}
+
+
+def run_reference(args, wl, ws_world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    t_small, f_small = _oracle_sample(wl, 128, 128)
+    # each step is a bounded sample; the whole run stays within a few minutes
+    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    side = int(128 * np.sqrt(max(1.0, min(64.0, per_step_budget / max(t_small, 1e-3)))))
+    for _ in range(args.warmup):
+        _oracle_sample(wl, side, side)
+    times, flops = [], []
+    for _ in range(args.steps):
+        t, f = _oracle_sample(wl, side, side)
+        times.append(t)
+        flops.append(f)
+    value = sum(flops) / sum(times) / 1e12
+    sample = "per expert: %d activation rows x %d weight rows, full K=%d" % (side, side, wl.K)
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * float(np.mean(times)), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": wl.name, "G": wl.G, "K": wl.K, "N": wl.N, "M": wl.M,
+                       "mode": wl.mode},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mxg", choices=["mxg", "reference"])
+    ap.add_argument("--config", default="mixtral_fprop_mxfp8")
+    ap.add_argument("--out", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "mxg":
+        args.warmup = 3
+    from moe_grouped_block_gb300 import workloads
+    wl = workloads.WORKLOADS[args.config]
+    ws_world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, wl, ws_world, rank)
+    else:
+        line = run_mxg(args, wl, ws_world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * mxg.h -- C ABI of the GB300 (sm_103a) grouped block-scaled quantize +
+ * grouped GEMM library (libmxg.so).
+ *
+ * The operations follow three public pages:
+ *   [TE-gemm]  TransformerEngine transformer_engine/jax/cpp_extensions/gemm.py
+ *              (commit 070b5b7): swizzled_scale, grouped_gemm,
+ *              _jax_scaled_matmul, _get_nvfp4_tensor_scale_inv.
+ *   [PR2763]   TransformerEngine PR #2763 "[JAX] MXFP8 Grouped Quant+GEMM".
+ *   [PR3661]   TransformerEngine PR #3661 "Add row-scaled NVFP4 support to
+ *              grouped-tensor GEMM".
+ *
+ * Conventions for every entry point
+ *   - All buffers are caller-owned DEVICE memory unless stated otherwise.
+ *     The library never allocates, frees or synchronises on these calls, so
+ *     each of them may be captured in a CUDA graph.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream).
+ *   - Host-detectable errors (null pointers, sizes, alignment, unsupported
+ *     combinations, a device that is not sm_103) are returned synchronously
+ *     and nothing is launched.  MXG_ERR_LAUNCH reports a failed launch.
+ *   - Data-dependent errors cannot be known on the host without a sync; the
+ *     kernels record them in a caller-owned sticky device word `dev_status`
+ *     (int32, atomicOr of the MXG_DEV_* bits) and clamp so that no access
+ *     leaves the buffers.  Read it after the stream or graph has completed.
+ *     `dev_status` may be NULL (then nothing is recorded).
+ *   - Rows are dense: a [rows, cols] matrix has leading dimension cols.
+ *   - bf16 is IEEE bfloat16 stored as uint16; E4M3 is the "fn" variant.
+ *   - The grouped matrices are 128-row aligned: every group size, K, N and
+ *     rows_capacity is a multiple of 128 (the alignment [PR2763] states for
+ *     the grouped quantize and GEMM setup kernels).
+ */
+#ifndef MXG_H_
+#define MXG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle (same type as cudaStream_t / CUstream). */
+struct CUstream_st;
+typedef struct CUstream_st* mxg_stream_t;
+
+typedef enum {
+  MXG_OK = 0,
+  MXG_ERR_INVALID_ARG = 1,         /* null pointer, bad size or enum value      */
+  MXG_ERR_ALIGNMENT = 2,           /* size not a multiple of 128, pointer not   */
+                                   /* 16-byte aligned                           */
+  MXG_ERR_UNSUPPORTED_ARCH = 3,    /* current device is not sm_103 (GB300)      */
+  MXG_ERR_LAUNCH = 4,              /* the CUDA launch failed                    */
+  MXG_ERR_WORKSPACE_TOO_SMALL = 5, /* workspace smaller than the size query     */
+  MXG_ERR_UNSUPPORTED = 6          /* valid but not implemented combination     */
+} mxg_status_t;
+
+/* Sticky device status bits (atomicOr into dev_status). */
+#define MXG_DEV_NEG_SIZE 1          /* a group size was negative: used as 0       */
+#define MXG_DEV_MISALIGNED 2        /* a group size was not a multiple of 128:    */
+                                    /* rounded down                               */
+#define MXG_DEV_SUM_OVER_CAPACITY 4 /* the sizes summed past rows_capacity: the   */
+                                    /* rows beyond it were dropped                */
+#define MXG_DEV_BOUNDS 8            /* an index check failed (debug builds)       */
+#define MXG_DEV_TIMEOUT 16          /* a pipeline wait ran out; the kernel gave   */
+                                    /* up on its tile and returned                */
+
+typedef enum {
+  MXG_MXFP8_E4M3 = 1,     /* E4M3 data, one E8M0 scale per 1x32 block          */
+  MXG_NVFP4_ROWSCALED = 2 /* E2M1 data, one E4M3 scale per 1x16 block, plus an  */
+                          /* FP32 outer scale per row                           */
+} mxg_format_t;
+
+typedef enum { MXG_ROWWISE = 1, MXG_COLWISE = 2, MXG_BOTH = 3 } mxg_qlayout_t;
+
+typedef enum {
+  MXG_FPROP_TN = 0, /* ragged output rows:  C[M_cap, N] = X[M_cap, K] . W[g]^T  */
+  MXG_WGRAD_NT = 1  /* ragged contraction:  dW[G, N, K] = dY_g^T . X_g          */
+} mxg_gemm_mode_t;
+
+typedef enum { MXG_OUT_F32 = 0, MXG_OUT_BF16 = 1 } mxg_out_t;
+
+/* One quantized GEMM operand: rowwise-quantized rows of the contraction dim.
+ *   data  : E4M3 bytes [rows, kdim] (MXFP8) or packed E2M1 [rows, kdim/2]
+ *           (NVFP4, element 2i in the low nibble of byte i).
+ *   scale : block scales in the swizzled layout of [TE-gemm] swizzled_scale
+ *           for the [rows, kdim/32] (MXFP8) or [rows, kdim/16] (NVFP4) scale
+ *           matrix: 128x4 tiles of 512 contiguous bytes, byte
+ *           ((r/128 * C/4 + c/4) * 32 + r%32) * 16 + (r%128)/32 * 4 + c%4.
+ *   outer : NVFP4 only: FP32 outer scale per row [rows]; NULL for MXFP8.
+ * data and scale must be 16-byte aligned. */
+typedef struct {
+  const void* data;
+  const uint8_t* scale;
+  const float* outer;
+} mxg_operand_t;
+
+/* ------------------------------------------------------------------------- */
+/* Group sizes -> int64 sizes + element offsets ([PR2763] description: int32 */
+/* sizes widened to int64 with a multiplier; offsets-kernel review thread:   */
+/* exclusive prefix sum of size * last_dim, G+1 values; workspace review     */
+/* thread: layout [G int64 sizes | G+1 int64 offsets]).                      */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of the offsets workspace: (2G + 1) * 8.  Returns 0 if G < 1. */
+size_t mxg_offsets_workspace_bytes(int G);
+
+/* sizes          : device int32[G] (sizes_is_int64 = 0) or int64[G] (= 1).
+ * multiplier     : rows per size unit (1 when sizes are row counts).
+ * last_dim       : elements per row, used for the element offsets.
+ * rows_capacity  : rows of the buffers the groups live in.
+ * ws             : device int64[2G+1]; written as
+ *                  ws[g] = s_g (sanitised rows of group g),
+ *                  ws[G] = 0, ws[G+1+g] = ws[G+g] + s_g * last_dim.
+ * Sanitisation (recorded in dev_status): a negative size counts as 0
+ * (NEG_SIZE); a size not a multiple of 128 is rounded down (MISALIGNED);
+ * rows past rows_capacity are dropped (SUM_OVER_CAPACITY).
+ * Errors: MXG_ERR_INVALID_ARG for null sizes/ws, G < 1 or G > 65536,
+ * multiplier < 1, last_dim < 1 or rows_capacity < 0. */
+mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int64_t multiplier,
+                               int64_t last_dim, int64_t rows_capacity, int64_t* ws,
+                               int32_t* dev_status, mxg_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Grouped quantize with the swizzled scale layout written directly         */
+/* ([PR2763] description: swizzle fused into the grouped quantize;          */
+/* [PR3661] description: row-scaled NVFP4 cast writes swizzled scales).     */
+/* ------------------------------------------------------------------------- */
+/* x             : bf16 [rows_capacity, cols], 16-byte aligned.
+ * group_ws      : offsets workspace from mxg_group_offsets (its first G
+ *                 entries are the rows of each group); the live rows are
+ *                 their sum, clamped to rows_capacity.  NULL: all
+ *                 rows_capacity rows are live (weights, [TE-gemm]
+ *                 grouped_gemm quantizes the kernel with no group sizes).
+ * Rows at or beyond the live count are neither read nor written.
+ *
+ * MXG_MXFP8_E4M3, rowwise (layout ROWWISE or BOTH):
+ *   q_row  : E4M3 [rows_capacity, cols]
+ *   sf_row : E8M0 swizzled [rows_capacity, cols/32]; group g's scales start
+ *            at byte row_off_g * cols / 32 ([PR2763]: scale offset = data
+ *            offset / 32).
+ *   Per 1x32 block: amax -> e = ceil(log2(amax / 448)) clamped to
+ *   [-127, 127] (all-zero block: e = -127), byte e + 127, data
+ *   E4M3_RNE(x * 2^-e).
+ * MXG_MXFP8_E4M3, colwise (layout COLWISE or BOTH), written transposed:
+ *   q_col  : E4M3 [cols, rows_capacity], q_col[k, m] = Q(x[m, k]) over
+ *            32x1 blocks along rows
+ *   sf_col : E8M0 swizzled [cols, rows_capacity/32] ([TE-gemm]
+ *            swizzled_scale, colwise: the scale matrix is transposed first).
+ * MXG_NVFP4_ROWSCALED (layout ROWWISE only):
+ *   q_row     : packed E2M1 [rows_capacity, cols/2]
+ *   sf_row    : E4M3 swizzled [rows_capacity, cols/16]
+ *   outer_row : FP32 [rows_capacity], s_r = amax_r / 2688
+ *               ([TE-gemm] _get_nvfp4_tensor_scale_inv: amax / (6 * 448)).
+ *   Per 1x16 block, fp32 round-to-nearest steps: S = 2688 / amax_r,
+ *   sb = E4M3_RNE_satfinite((amax_b / 6) * S), code =
+ *   E2M1_RNE_satfinite(x * (S / sb)) (signed zeros when sb or amax_r is 0).
+ * Unused output pointers may be NULL.
+ * Errors: INVALID_ARG (null required pointer, bad enum, NVFP4 with a colwise
+ * layout), ALIGNMENT (rows_capacity or cols not a multiple of 128, pointer
+ * not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
+mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const void* x,
+                                int64_t rows_capacity, int64_t cols, const int64_t* group_ws,
+                                int G, void* q_row, uint8_t* sf_row, void* q_col, uint8_t* sf_col,
+                                float* outer_row, int32_t* dev_status, mxg_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Grouped block-scaled GEMM ([TE-gemm] grouped_gemm; [PR2763] V2 grouped    */
+/* GEMM consuming pre-swizzled scales; [PR3661] row-scaled NVFP4: neutral    */
+/* outer scales, FP32 accumulation, outer scales applied afterwards).       */
+/* ------------------------------------------------------------------------- */
+/* MXG_FPROP_TN (ragged rows):
+ *   A = activations, rowwise: data [M_cap, K]; B = weights, rowwise:
+ *   data [G*N, K] (expert g owns rows g*N .. g*N+N-1).
+ *   C[off_g + i, n] = alpha_g * sum_k A[off_g+i, k] * B[g*N+n, k]
+ *                     + beta_g * C[off_g + i, n];   C is [M_cap, N].
+ *   Rows of C at or beyond the live count are not written.
+ *   NVFP4: A.outer [M_cap] and B.outer [G*N] are required, and the result is
+ *   multiplied by A.outer[row] * B.outer[g*N + n].
+ * MXG_WGRAD_NT (ragged contraction, MXFP8):
+ *   A = colwise copy of dY: data [N, M_cap], scale [N, M_cap/32];
+ *   B = colwise copy of X:  data [K, M_cap], scale [K, M_cap/32].
+ *   dW[g, n, k] = alpha_g * sum_{m in group g} A[n, m] * B[k, m]
+ *                 + beta_g * dW[g, n, k];   C = dW is [G, N, K].
+ *   An empty group writes beta_g * dW[g] (zeros when beta is NULL).
+ * group_ws : offsets workspace of mxg_group_offsets (first G entries used).
+ * alpha, beta : device float[G] or NULL (alpha = 1, beta = 0).
+ * workspace : not needed by this implementation (size query returns 0);
+ *             may be NULL.
+ * Accumulation is FP32 in tensor memory; the FP32 output is the parity
+ * output, bf16 is rounded to nearest even from it.
+ * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 wgrad, beta with
+ * NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
+ * 128; data/scale/C not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
+mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                              const mxg_operand_t* B, const int64_t* group_ws, int G,
+                              int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                              const float* beta, void* C, mxg_out_t out_type, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, mxg_stream_t stream);
+
+/* Workspace bytes mxg_grouped_gemm needs (0 for every combination here). */
+size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,
+                                        int64_t M_cap, int64_t N);
+
+/* ------------------------------------------------------------------------- */
+/* Dequantize ([PR2763] dequantizer: inverse swizzle of the scales, then    */
+/* data * scale).  Test helper; not on the timed path.                      */
+/* ------------------------------------------------------------------------- */
+/* ROWWISE: q [rows, cols] (NVFP4: [rows, cols/2]), sf swizzled [rows,
+ *          cols/32 or cols/16], outer [rows] (NVFP4) -> out [rows, cols].
+ * COLWISE: (MXFP8 only) q is the transposed copy [cols, rows], sf swizzled
+ *          [cols, rows/32] -> out [rows, cols] (transposed back).
+ * out is FP32 or bf16 (round to nearest even).
+ * Errors: INVALID_ARG, ALIGNMENT (rows or cols not multiples of 128),
+ * UNSUPPORTED (NVFP4 colwise), UNSUPPORTED_ARCH, LAUNCH. */
+mxg_status_t mxg_dequantize(mxg_format_t fmt, mxg_qlayout_t layout, const void* q,
+                            const uint8_t* sf, const float* outer, int64_t rows, int64_t cols,
+                            void* out, mxg_out_t out_type, mxg_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mxg_status_string(mxg_status_t status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int mxg_version(void);
+
+/* Number of kernel launches this library has issued in this process
+ * (all entry points, all devices).  For launch accounting in benchmarks. */
+uint64_t mxg_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXG_H_ */

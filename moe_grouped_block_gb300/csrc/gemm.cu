@@ -1,0 +1,542 @@
+// gemm.cu -- persistent grouped block-scaled GEMM on tcgen05 (sm_103a).
+//
+// What it computes (TransformerEngine gemm.py grouped_gemm and PR #2763's V2
+// grouped GEMM; PR #3661 for the row-scaled NVFP4 variant):
+//   fprop TN (ragged rows):        C[off_g+i, n] = alpha_g * sum_k A[off_g+i, k] B[g*N+n, k]
+//   wgrad NT (ragged contraction): dW[g, n, k]   = alpha_g * sum_{m in g} A[n, m] B[k, m]
+// (+ beta_g * previous C), with E4M3 x E8M0/1x32 (MXFP8) or E2M1 x
+// E4M3/1x16 (NVFP4) operands whose scales arrive pre-swizzled from the
+// grouped quantize, FP32 accumulation in tensor memory and an epilogue that
+// applies alpha, beta and -- for NVFP4 -- the per-row / per-column FP32
+// outer scales (PR #3661 runs the GEMM with neutral outer scales into an FP32
+// scratch and scales afterwards; here the scratch is tensor memory and the
+// scaling is fused into the read-out).
+//
+// Design (GB300-first, no library):
+//   * one CTA per SM, persistent; tiles are walked in a static round-robin
+//     order derived on the device from the offsets workspace, so there is no
+//     host sync and the launch is graph-safe (PR #2763's motivation).
+//   * warp 0 lane 0: TMA producer (A and B tiles with the 128-byte swizzle,
+//     scale tiles as plain bulk copies); warp 1 lane 0: MMA issuer;
+//     warps 2..: epilogue, one TMEM lane quarter and 128 columns each.
+//   * tile 128 x BN, 128 bytes of K per pipeline stage = 4 MMAs of 32 bytes
+//     (32 E4M3 or 64 E2M1 elements each).
+//   * scales: each 128x4 swizzled scale tile (512 bytes) is copied into 4
+//     TMEM columns by tcgen05.cp 32x128b.warpx4 -- the swizzled layout is
+//     exactly the one that copy and the block-scaled MMA consume.  Each
+//     pipeline stage owns its own scale columns, so refilling a stage never
+//     races an MMA that still reads the previous scales.
+//   * fprop orders tiles group-major, then n, then m: the CTAs in flight
+//     share one weight tile and the group's activations stay in L2.
+//   * every mbarrier wait is bounded (mbar_wait); after a timeout the CTA
+//     drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "mxg_device.cuh"
+
+namespace mxg {
+
+struct GemmParams {
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const float* a_outer;
+  const float* b_outer;
+  const int64_t* group_ws;
+  const float* alpha;
+  const float* beta;
+  void* C;
+  int32_t* status;
+  int64_t M_cap, N, K;
+  int64_t atoms_row;  // 512-byte scale tiles per 128-row band of an operand
+  int64_t kb_fprop;   // K blocks (128 bytes) of one fprop tile
+  int G;
+  int mode;  // 0 fprop, 1 wgrad
+  int out_bf16;
+};
+
+template <int BN, int STAGES, int ACC, bool NVF4>
+struct GemmCfg {
+  static constexpr int kEpiWarps = 4 * (BN / 128);
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kATile = 128 * 128;
+  static constexpr int kBTile = BN * 128;
+  static constexpr int kAtomsK = NVF4 ? 4 : 1;  // scale tiles along K per stage and band
+  static constexpr int kSfaBytes = 512 * kAtomsK;
+  static constexpr int kSfbBytes = 512 * kAtomsK * (BN / 128);
+  static constexpr int kStageBytes =
+      ((kATile + kBTile + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
+  static constexpr uint32_t kTxBytes = kATile + kBTile + kSfaBytes + kSfbBytes;
+  static constexpr int kSfaCols = 4 * kAtomsK;
+  static constexpr int kSfCols = kSfaCols * (1 + BN / 128);  // TMEM columns per stage
+  static constexpr int kTmemCols = 512;
+  static_assert(ACC * BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
+  // barriers: full[S], empty[S], tfull[ACC], tempty[ACC], drain; then the
+  // TMEM base address and the abort flag
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 2 * ACC + 1) + 16;
+  static size_t smem_bytes(int G) {
+    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 8 * (G + 1) + 16;
+  }
+  // Instruction descriptor: A/B formats at bits 7 / 10 (E4M3 = 0 for
+  // mxf8f6f4, E2M1 = 1 for mxf4nvf4), N >> 3 at bit 17, scale format at bit
+  // 23 (1 = UE8M0, 0 = UE4M3), M >> 4 at bit 24; K-major A and B; scale
+  // data ids at bits 4 (B) and 29 (A) are added per MMA.
+  static constexpr uint32_t kIdesc = (NVF4 ? ((1u << 7) | (1u << 10)) : 0u) |
+                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (NVF4 ? 0u : (1u << 23)) | ((128u >> 4) << 24);
+};
+
+struct TileInfo {
+  int g;
+  int64_t a_row, b_row;      // first row of the A / B tile (TMA coordinate 1)
+  int64_t kb_begin, kb_end;  // K blocks of 128 bytes
+  int64_t c_row, c_col;      // top-left output element
+  int64_t row_end;           // rows of C at or beyond this are not written
+};
+
+template <int BN>
+__device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, const int32_t* row_off,
+                                             const int32_t* tile_off) {
+  TileInfo ti;
+  if (p.mode == 0) {
+    int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_off[mid] <= t)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int g = lo;
+    const int64_t mt = (row_off[g + 1] - row_off[g]) >> 7;
+    const int64_t local = t - tile_off[g];
+    const int64_t n_tile = local / mt, m_tile = local % mt;
+    ti.g = g;
+    ti.a_row = row_off[g] + 128 * m_tile;
+    ti.b_row = static_cast<int64_t>(g) * p.N + BN * n_tile;
+    ti.kb_begin = 0;
+    ti.kb_end = p.kb_fprop;
+    ti.c_row = ti.a_row;
+    ti.c_col = BN * n_tile;
+    ti.row_end = row_off[g + 1];
+  } else {
+    const int64_t kt = p.K / BN, tpg = (p.N >> 7) * kt;
+    const int g = static_cast<int>(t / tpg);
+    const int64_t local = t % tpg;
+    const int64_t n_tile = local / kt, k_tile = local % kt;
+    ti.g = g;
+    ti.a_row = 128 * n_tile;
+    ti.b_row = BN * k_tile;
+    ti.kb_begin = row_off[g] >> 7;
+    ti.kb_end = row_off[g + 1] >> 7;
+    ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
+    ti.c_col = ti.b_row;
+    ti.row_end = static_cast<int64_t>(g + 1) * p.N;
+  }
+  return ti;
+}
+
+// Bounded wait used only while tearing down: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, int32_t* status) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      status_set(status, MXG_DEV_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int BN, int STAGES, int ACC, bool NVF4>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 2 * ACC + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
+  int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
+  int32_t* tile_off = row_off + (p.G + 1);
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint32_t smem_base = smem_u32(smem);
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + ACC + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 2 * ACC]);
+
+  // ------------------------------------------------------------ set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), Cfg::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_base_s), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 1) {
+    // group tables: sanitised row offsets and tile offsets (fprop)
+    int64_t carry_rows = 0, carry_tiles = 0;
+    int32_t bits = 0;
+    const int64_t ntiles_n = p.N / BN;
+    for (int base = 0; base < p.G; base += 32) {
+      const int g = base + static_cast<int>(lane);
+      int64_t s = 0;
+      if (g < p.G) {
+        s = p.group_ws[g];
+        if (s < 0) {
+          s = 0;
+          bits |= MXG_DEV_NEG_SIZE;
+        }
+        if (s & 127) {
+          s &= ~static_cast<int64_t>(127);
+          bits |= MXG_DEV_MISALIGNED;
+        }
+        if (s > p.M_cap) s = p.M_cap;
+      }
+      int64_t incl = s;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= static_cast<uint32_t>(d)) incl += v;
+      }
+      const int64_t before = min(carry_rows + incl - s, p.M_cap);
+      const int64_t after = min(carry_rows + incl, p.M_cap);
+      if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
+      const int64_t tiles_g = p.mode == 0 ? ((after - before) >> 7) * ntiles_n : 0;
+      int64_t tincl = tiles_g;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t v = __shfl_up_sync(0xFFFFFFFFu, tincl, d);
+        if (lane >= static_cast<uint32_t>(d)) tincl += v;
+      }
+      if (g < p.G) {
+        row_off[g] = static_cast<int32_t>(before);
+        tile_off[g] = static_cast<int32_t>(carry_tiles + tincl - tiles_g);
+      }
+      carry_rows += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      carry_tiles += __shfl_sync(0xFFFFFFFFu, tincl, 31);
+    }
+    if (lane == 0) {
+      row_off[p.G] = static_cast<int32_t>(min(carry_rows, p.M_cap));
+      tile_off[p.G] = static_cast<int32_t>(carry_tiles);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, d);
+    if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_s;
+  const int64_t total_tiles =
+      p.mode == 0 ? static_cast<int64_t>(tile_off[p.G]) : p.G * (p.N >> 7) * (p.K / BN);
+
+  // ------------------------------------------------------------ producer
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmap_a);
+      prefetch_tmap(&tmap_b);
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, last_parity = 0;  // per stage, for the final drain
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+        for (int64_t kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sb = sa + Cfg::kATile;
+          const uint32_t ssfa = sb + Cfg::kBTile;
+          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+          tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(kb * 128), static_cast<int32_t>(ti.a_row));
+          tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kb * 128), static_cast<int32_t>(ti.b_row));
+          const int64_t katom = kb * Cfg::kAtomsK;
+          bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.atoms_row + katom) * 512, Cfg::kSfaBytes, fb);
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+            bulk_load(ssfb + i * 512 * Cfg::kAtomsK,
+                      p.b_sf + (((ti.b_row >> 7) + i) * p.atoms_row + katom) * 512,
+                      512 * Cfg::kAtomsK, fb);
+          issued_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every copy this thread issued has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u, p.status);
+    }
+  }
+  // ------------------------------------------------------------ MMA issuer
+  else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int64_t kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sb = sa + Cfg::kATile;
+          const uint32_t ssfa = sb + Cfg::kBTile;
+          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+          const uint32_t sfa_t = tmem_base + ACC * BN + stage * Cfg::kSfCols;
+          const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          // scale tiles -> TMEM.  A: tile a at column 4a.  B: for K-step a,
+          // band i at column a * 4 * (BN/128) + 4i (the bands of one MMA are
+          // adjacent, 4 columns each).
+#pragma unroll
+          for (int a = 0; a < Cfg::kAtomsK; ++a)
+            tc_cp_scales(sfa_t + 4 * a, smem_desc(ssfa + 512 * a, 0, 128, 0));
+#pragma unroll
+          for (int i = 0; i < BN / 128; ++i)
+#pragma unroll
+            for (int a = 0; a < Cfg::kAtomsK; ++a)
+              tc_cp_scales(sfb_t + a * 4 * (BN / 128) + 4 * i,
+                           smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc(sa + 32 * kk, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, 1024, 2);
+            const uint32_t accum = (kb > ti.kb_begin || kk > 0) ? 1u : 0u;
+            if (NVF4) {
+              tc_mma_nvf4(d_tmem, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
+                          sfb_t + kk * 4 * (BN / 128), accum);
+            } else {
+              const uint32_t idesc = Cfg::kIdesc | (static_cast<uint32_t>(kk) << 4) |
+                                     (static_cast<uint32_t>(kk) << 29);
+              tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, accum);
+            }
+          }
+          tc_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));  // accumulator ready (immediately if no K blocks)
+        if (++acc == ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs this thread issued have completed before TMEM is freed
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0, p.status);
+    }
+  }
+  // ------------------------------------------------------------ epilogue
+  else {
+    const uint32_t ew = warp - 2;
+    const uint32_t quarter = warp & 3u;  // TMEM lanes 32*quarter .. +31
+    const uint32_t col0 = 128u * (ew >> 2);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+      const bool has_k = ti.kb_end > ti.kb_begin;
+      if (has_k) {
+        const uint32_t taddr = tmem_base + ((32u * quarter) << 16) + acc * BN + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, v[c]);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+
+      const int64_t row = ti.c_row + 32 * quarter + lane;
+      if (row < ti.row_end) {
+        const int64_t ldc = p.mode == 0 ? p.N : p.K;
+        const int64_t cbase = row * ldc + ti.c_col + col0;
+        const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
+        const float beta = p.beta ? p.beta[ti.g] : 0.0f;
+        float rs = 1.0f;
+        const float* cs = nullptr;
+        if (NVF4) {
+          rs = p.a_outer[row];
+          cs = p.b_outer + ti.b_row + col0;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a = has_k ? __uint_as_float(v[c][4 * q4 + e]) : 0.0f;
+              if (NVF4) a = a * rs * cs[32 * c + 4 * q4 + e];
+              o[e] = alpha * a;
+            }
+            const int64_t idx = cbase + 32 * c + 4 * q4;
+            if (beta != 0.0f) {
+              if (p.out_bf16) {
+                const uint2 old = *reinterpret_cast<const uint2*>(static_cast<uint16_t*>(p.C) + idx);
+                o[0] += beta * bf16lo(old.x);
+                o[1] += beta * bf16hi(old.x);
+                o[2] += beta * bf16lo(old.y);
+                o[3] += beta * bf16hi(old.y);
+              } else {
+                const float4 old = *reinterpret_cast<const float4*>(static_cast<float*>(p.C) + idx);
+                o[0] += beta * old.x;
+                o[1] += beta * old.y;
+                o[2] += beta * old.z;
+                o[3] += beta * old.w;
+              }
+            }
+            if (p.out_bf16) {
+              uint2 w;
+              w.x = f32_to_bf16_bits(o[0]) | (f32_to_bf16_bits(o[1]) << 16);
+              w.y = f32_to_bf16_bits(o[2]) | (f32_to_bf16_bits(o[3]) << 16);
+              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.C) + idx) = w;
+            } else {
+              *reinterpret_cast<float4*>(static_cast<float*>(p.C) + idx) =
+                  make_float4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows, inner_bytes], box [box_rows, 128 bytes], 128-byte
+// swizzle (the layout the K-major MMA descriptors above describe).
+bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows,
+               uint32_t box_rows) {
+  auto enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner_bytes, rows};
+  const cuuint64_t strides[1] = {inner_bytes};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int ACC, bool NVF4>
+cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                           int64_t max_tiles, int num_sms, cudaStream_t stream) {
+  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4>;
+  const size_t smem = Cfg::smem_bytes(p.G);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Tile width: 256 when the output tile dimension allows it (one accumulator
+// stage, 8 epilogue warps), else 128 (two accumulator stages).  The
+// environment variable MXG_GEMM_TILE_N=128 forces the narrow tile.
+cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const uint8_t* a_sf,
+                                const float* a_outer, const void* b_data, const uint8_t* b_sf,
+                                const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
+                                int64_t N, int64_t K, const float* alpha, const float* beta,
+                                void* C, int out_bf16, int32_t* status, int num_sms, int tile_n,
+                                cudaStream_t stream) {
+  GemmParams p;
+  p.a_sf = a_sf;
+  p.b_sf = b_sf;
+  p.a_outer = a_outer;
+  p.b_outer = b_outer;
+  p.group_ws = group_ws;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.C = C;
+  p.status = status;
+  p.M_cap = M_cap;
+  p.N = N;
+  p.K = K;
+  p.G = G;
+  p.mode = mode;
+  p.out_bf16 = out_bf16;
+  const int64_t kdim = mode == 0 ? K : M_cap;                 // contraction length
+  p.atoms_row = nvfp4 ? kdim / 64 : kdim / 128;               // (kdim/blk)/4 scale tiles
+  p.kb_fprop = nvfp4 ? K / 256 : K / 128;                     // 128-byte K blocks
+  const int64_t out_cols = mode == 0 ? N : K;
+  const int bn = (tile_n == 128 || out_cols % 256 != 0) ? 128 : 256;
+
+  const uint64_t kbytes = nvfp4 ? static_cast<uint64_t>(kdim / 2) : static_cast<uint64_t>(kdim);
+  CUtensorMap ta, tb;
+  const uint64_t a_rows = mode == 0 ? M_cap : N;
+  const uint64_t b_rows = mode == 0 ? static_cast<uint64_t>(G) * N : K;
+  if (!make_tmap(&ta, a_data, kbytes, a_rows, 128) || !make_tmap(&tb, b_data, kbytes, b_rows, bn))
+    return cudaErrorInvalidValue;
+
+  const int64_t max_tiles = mode == 0 ? (M_cap / 128) * (N / bn) : G * (N / 128) * (K / bn);
+  if (nvfp4) {
+    if (bn == 256) return launch_variant<256, 4, 1, true>(ta, tb, p, max_tiles, num_sms, stream);
+    return launch_variant<128, 5, 2, true>(ta, tb, p, max_tiles, num_sms, stream);
+  }
+  if (bn == 256) return launch_variant<256, 4, 1, false>(ta, tb, p, max_tiles, num_sms, stream);
+  return launch_variant<128, 6, 2, false>(ta, tb, p, max_tiles, num_sms, stream);
+}
+
+}  // namespace mxg

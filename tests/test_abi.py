@@ -1,0 +1,102 @@
+"""The C-ABI library loads, exports every function include/mxg.h declares,
+and rejects bad arguments synchronously -- all without a GPU.  Every call
+below fails validation before any device work, so it is safe anywhere."""
+import ctypes
+
+import pytest
+import torch
+
+from moe_grouped_block_gb300 import build as mxg_build
+from moe_grouped_block_gb300 import mxg
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mxg_build.build()
+    return mxg.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = mxg.declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), "libmxg.so does not export " + n
+
+
+def test_scalar_queries(lib):
+    assert mxg.mxg_offsets_workspace_bytes(8) == (2 * 8 + 1) * 8
+    assert mxg.mxg_offsets_workspace_bytes(0) == 0
+    assert mxg.mxg_grouped_gemm_workspace_bytes(1, 0, 8, 16384, 14336) == 0
+    assert mxg.mxg_version() >= 100
+    for code, name in mxg.STATUS_NAMES.items():
+        assert mxg.mxg_status_string(code) == name
+    assert mxg.mxg_status_string(99) == "MXG_ERR_UNKNOWN"
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null value; never dereferenced (validation fails first)
+
+
+def test_offsets_argument_errors(lib):
+    L = lib
+    assert L.mxg_group_offsets(None, 0, 4, 1, 128, 512, FAKE, None, None) == 1
+    assert L.mxg_group_offsets(FAKE, 0, 0, 1, 128, 512, FAKE, None, None) == 1
+    assert L.mxg_group_offsets(FAKE, 0, 4, 0, 128, 512, FAKE, None, None) == 1
+    assert L.mxg_group_offsets(FAKE, 0, 4, 1, 0, 512, FAKE, None, None) == 1
+    assert L.mxg_group_offsets(FAKE, 0, 4, 1, 128, -1, None, None, None) == 1
+
+
+def test_quantize_argument_errors(lib):
+    L = lib
+    q = L.mxg_group_quantize
+    # bad format / layout
+    assert q(7, 1, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
+    assert q(1, 4, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
+    # missing outputs
+    assert q(1, 3, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
+    # NVFP4 colwise is not part of the row-scaled path
+    assert q(2, 2, FAKE, 128, 128, None, 1, None, None, FAKE, FAKE, FAKE, None, None) == 1
+    # sizes not multiples of 128, misaligned pointer
+    assert q(1, 1, FAKE, 100, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
+    assert q(1, 1, FAKE, 128, 96, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
+    assert q(1, 1, FAKE + 8, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
+
+
+def test_gemm_argument_errors(lib):
+    L = lib
+    op = mxg.Operand(FAKE, FAKE, None)
+    opo = mxg.Operand(FAKE, FAKE, FAKE)
+    r = ctypes.byref
+    g = L.mxg_grouped_gemm
+    assert g(1, 0, None, r(op), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), None, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), FAKE, 0, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), FAKE, 1025, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 5, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    # NVFP4: wgrad, beta and missing outer scales are rejected
+    assert g(2, 1, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, FAKE, FAKE, 0, None, 0, None, None) == 1
+    assert g(2, 0, r(op), r(opo), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    # alignment
+    assert g(1, 0, r(op), r(op), FAKE, 4, 500, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 200, 256, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 384, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, FAKE + 4, 0, None, 0, None, None) == 2
+
+
+def test_dequantize_argument_errors(lib):
+    L = lib
+    assert L.mxg_dequantize(1, 1, None, FAKE, None, 128, 128, FAKE, 0, None) == 1
+    assert L.mxg_dequantize(2, 2, FAKE, FAKE, FAKE, 128, 128, FAKE, 0, None) == 6
+    assert L.mxg_dequantize(1, 1, FAKE, FAKE, None, 120, 128, FAKE, 0, None) == 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_no_device_is_reported_not_launched(lib):
+    # valid arguments but no usable device: refused before any launch
+    assert lib.mxg_group_offsets(FAKE, 0, 4, 1, 128, 512, FAKE, None, None) == 3
+
+
+def test_binding_refuses_host_tensors(lib):
+    with pytest.raises(ValueError):
+        mxg.mxg_group_offsets(torch.zeros(4, dtype=torch.int32), 1, 128, 512,
+                              torch.zeros(9, dtype=torch.int64))

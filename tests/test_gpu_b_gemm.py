@@ -1,0 +1,185 @@
+"""GPU parity: the grouped block-scaled GEMM through the C ABI against the
+oracle's fp64 per-expert GEMM over the oracle's own quantized operands.
+
+Tolerance: max |C - R| / max |R| <= 1e-3 per expert (the normwise reading of
+"max relative error 1e-3"); FP32 accumulation over K <= 4096 products of
+exactly-representable values sits near 1e-6, so 1e-3 leaves the margin the
+statement allows.  bf16 output is compared with the oracle rounded to bf16,
+within one bf16 ulp.  The quantized operands are also checked bit-exact
+against the oracle here, so a GEMM failure is never a quantize failure."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_grouped_block_gb300 import mxg, workloads
+
+from gpu_util import (DEV, fprop_case, gpu_mxfp8, gpu_offsets, normwise_errors, oracle_fprop,
+                      oracle_quantized_operands, require_gpu, tile_n, u8)
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _assert_operands_match(case, a, b, live):
+    assert np.array_equal(case["qx"]["q_row"][:live].cpu().numpy(), a["q"][:live])
+    assert np.array_equal(case["qw"]["q_row"].cpu().numpy(), b["q"])
+    assert np.array_equal(u8(case["qw"]["sf_row"]), b["sf"])
+
+
+def _run_fprop(wl, tn=None, **kw):
+    with tile_n(tn):
+        case = fprop_case(wl, **kw)
+    offs, rows, cols, ref, a, b = oracle_fprop(wl, case["inp"], alpha=kw.get("alpha"),
+                                               beta=kw.get("beta"),
+                                               c_in=None if kw.get("c_in") is None else
+                                               kw["c_in"].double().numpy())
+    _assert_operands_match(case, a, b, int(offs[-1]))
+    assert int(case["status"].item()) == 0
+    return case, offs, rows, ref
+
+
+def test_single_tile_one_hot():
+    # one expert, one 128x128 tile, one K block: C[m, n] = W[n, m] exactly
+    G, N, K, M = 1, 128, 128, 128
+    xf = torch.zeros((M, K))
+    xf[torch.arange(M), torch.arange(M)] = 1.0
+    wl = workloads.Workload("one_hot", "fprop", "mxfp8", G, K, N, M, 0, "fixed", (M,))
+    w = torch.randint(-8, 9, (G, N, K)).float()
+    inp = {"x": xf.to(torch.bfloat16), "w": w.to(torch.bfloat16),
+           "sizes": torch.tensor([M], dtype=torch.int32)}
+    x = inp["x"].to(DEV)
+    ws, st = gpu_offsets(inp["sizes"], K, M)
+    qx, _ = gpu_mxfp8(x, ws, G, mxg.MXG_ROWWISE)
+    qw, _ = gpu_mxfp8(inp["w"].to(DEV).reshape(N, K), None, 1, mxg.MXG_ROWWISE)
+    C = torch.full((M, N), 7.0, device=DEV)
+    mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, (qx["q_row"], qx["sf_row"], None),
+                         (qw["q_row"], qw["sf_row"], None), ws, G, M, N, K, C=C, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(C.cpu(), w[0].t().contiguous())
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_fprop_tiny_workload(tn):
+    wl = workloads.WORKLOADS["tiny_fprop_mxfp8"]
+    case, offs, rows, ref = _run_fprop(wl, tn)
+    got = case["C"].cpu().numpy().astype(np.float64)
+    errs = normwise_errors(got[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_fprop_mixtral_shape_scaled(tn):
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=2048, K=512, N=512)
+    case, offs, rows, ref = _run_fprop(wl, tn)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+def test_fprop_finegrained_empty_groups():
+    wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=4096, K=256)
+    inp_sizes = workloads.group_sizes(wl)
+    assert (inp_sizes == 0).any()
+    case, offs, rows, ref = _run_fprop(wl)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+def test_fprop_alpha_beta_and_capacity_padding():
+    wl = workloads.WORKLOADS["tiny_fprop_mxfp8"].scaled(M_cap=768)
+    G, N = wl.G, wl.N
+    c_in = torch.linspace(-1, 1, 768 * N).reshape(768, N).float()
+    alpha = [1.0, 3.0, -0.5, 0.125]
+    beta = [0.0, 1.0, 2.0, -1.0]
+    case, offs, rows, ref = _run_fprop(wl, alpha=alpha, beta=beta, c_in=c_in)
+    got = case["C"].cpu().numpy().astype(np.float64)
+    errs = normwise_errors(got[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+    # rows beyond the live count keep their previous contents
+    assert np.array_equal(got[wl.M:], c_in.numpy()[wl.M:].astype(np.float64))
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_fprop_bf16_output(tn):
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=256, N=512)
+    case, offs, rows, ref = _run_fprop(wl, tn, out_type=mxg.MXG_OUT_BF16)
+    got = case["C"].cpu().float().numpy().astype(np.float64)[:wl.M]
+    refb = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    ulp = np.abs(refb) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(got - refb) <= ulp + 1e-6 * np.abs(ref).max())
+
+
+# --------------------------------------------------------------------------- wgrad
+def _wgrad_case(wl, tn=None, beta=None):
+    inp = workloads.make_inputs(wl)
+    G, N, K, M = wl.G, wl.N, wl.K, wl.rows_capacity
+    ws, st = gpu_offsets(inp["sizes"], K, M)
+    qx, _ = gpu_mxfp8(inp["x"].to(DEV), ws, G, mxg.MXG_COLWISE)
+    qd, _ = gpu_mxfp8(inp["dy"].to(DEV), ws, G, mxg.MXG_COLWISE)
+    c0 = torch.linspace(-2, 2, G * N * K).reshape(G, N, K).float()
+    dW = c0.to(DEV).clone()
+    be = None if beta is None else torch.tensor(beta, dtype=torch.float32, device=DEV)
+    with tile_n(tn):
+        mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_WGRAD_NT, (qd["q_col"], qd["sf_col"], None),
+                             (qx["q_col"], qx["sf_col"], None), ws, G, M, N, K, None, be, dW,
+                             dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # oracle on its own colwise quantization
+    rws, _ = oracle.group_offsets(inp["sizes"].numpy(), 1, K, M)
+    offs = oracle.live_rows(rws, G)
+    live = int(offs[-1])
+    ox = oracle.mxfp8_quantize(inp["x"], live, M, rowwise=False, colwise=True)
+    od = oracle.mxfp8_quantize(inp["dy"], live, M, rowwise=False, colwise=True)
+    assert np.array_equal(qx["q_col"][:, :live].cpu().numpy(), ox["q_col"][:, :live])
+    assert np.array_equal(qd["q_col"][:, :live].cpu().numpy(), od["q_col"][:, :live])
+    _, _, ref = oracle.grouped_gemm_wgrad({"q": od["q_col"], "sf": od["sf_col"]},
+                                          {"q": ox["q_col"], "sf": ox["sf_col"]}, offs, M, N, K,
+                                          beta=beta, c_in=c0.double().numpy())
+    return dW.cpu().numpy().astype(np.float64), ref, offs
+
+
+@pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (128, 512)])
+def test_wgrad_scaled(tn, K):
+    wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=2048, K=K, N=256)
+    sizes = workloads.group_sizes(wl)
+    got, ref, offs = _wgrad_case(wl, tn)
+    for g in range(wl.G):
+        den = np.abs(ref[g]).max()
+        if sizes[g] == 0:
+            assert not got[g].any(), "empty group must be zero-filled"
+        else:
+            assert np.abs(got[g] - ref[g]).max() / den <= TOL
+
+
+def test_wgrad_empty_group_beta():
+    wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=1024, K=256, N=256, sizes="fixed",
+                                                     fixed_sizes=(256, 0, 512, 0, 128, 128, 0, 0))
+    beta = [0.0, 1.0, 0.5, -1.0, 2.0, 0.0, 0.0, 3.0]
+    got, ref, offs = _wgrad_case(wl, beta=beta)
+    for g in range(wl.G):
+        den = max(np.abs(ref[g]).max(), 1e-30)
+        assert np.abs(got[g] - ref[g]).max() / den <= TOL, g
+
+
+# --------------------------------------------------------------------------- NVFP4
+@pytest.mark.parametrize("tn", [None, 128])
+def test_nvfp4_fprop_scaled(tn):
+    wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=4096, K=512, N=512)
+    case, offs, rows, ref = _run_fprop(wl, tn)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+def test_nvfp4_fprop_alpha():
+    wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=1024, K=256, N=256, G=4)
+    alpha = [1.0, -2.0, 0.5, 4.0]
+    case, offs, rows, ref = _run_fprop(wl, alpha=alpha)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
