@@ -51,6 +51,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """MAX of a per-rank scalar over all ranks (identity without a group)."""
+    if dist is None or not dist.is_initialized():
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_workload(wl, rank: int):
+    """Each rank runs an independent replica on its own seeded batch."""
+    return wl if rank == 0 else wl.scaled(seed=wl.seed + 1000 * rank)
+
+
+def job_tflops(flop_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the FLOP of all ranks over the slowest rank's time."""
+    return world * flop_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -116,15 +136,13 @@ class ClockSampler:
 class Path:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, wl, out_bf16: bool, dev, seed_offset: int = 0):
+    def __init__(self, wl, out_bf16: bool, dev, rank: int = 0):
         import torch
         from moe_grouped_block_gb300 import mxg, workloads
         self.mxg, self.torch = mxg, torch
         self.wl = wl
         self.dev = dev
-        if seed_offset:
-            wl = wl.scaled(seed=wl.seed + 1000 * seed_offset)
-        inp = workloads.make_inputs(wl)
+        inp = workloads.make_inputs(replica_workload(wl, rank))
         self.host = inp
         G, N, K, R = wl.G, wl.N, wl.K, wl.rows_capacity
         self.G, self.N, self.K, self.R = G, N, K, R
@@ -230,6 +248,40 @@ class Path:
         return [("sizes", self.sizes), ("x", self.x), ("dy", self.dy)]
 
 
+def measure_e2e(path, step, args, dist, dev, flush, stream):
+    """The step through the same C-ABI calls with host buffers: every step
+    copies its inputs from pinned host memory to the device and its output
+    back, inside the timed region.  Returns (ms per step, H2D bytes, D2H bytes)."""
+    import torch
+    host_in = [(n, t.cpu().pin_memory()) for n, t in path.input_tensors()]
+    host_out = torch.empty(path.C.shape, dtype=path.C.dtype).pin_memory()
+    dev_in = dict(path.input_tensors())
+    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for n, t in host_in:
+            dev_in[n].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(path.C, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    for e0, e1 in ev:
+        flush.fill_(1.0)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), dist, dev)
+    return ms, h2d, d2h
+
+
 def run_mxg(args, wl, ws_world, rank, local):
     import torch
     from moe_grouped_block_gb300 import mxg
@@ -239,7 +291,7 @@ def run_mxg(args, wl, ws_world, rank, local):
     if ws_world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    path = Path(wl, args.out == "bf16", dev, seed_offset=rank)
+    path = Path(wl, args.out == "bf16", dev, rank=rank)
     stages = path.stages()
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -281,45 +333,13 @@ def run_mxg(args, wl, ws_world, rank, local):
     per_kernel = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
                   for i, (name, _) in enumerate(stages)}
     step_ms = [ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]
-    ms = float(np.mean(step_ms))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
     if int(path.status.item()) != 0:
         raise RuntimeError("device status %d" % int(path.status.item()))
 
     # ---- e2e: host buffers, copies inside the timed region
-    host_in = [(n, t.cpu().pin_memory()) for n, t in path.input_tensors()]
-    host_out = torch.empty(path.C.shape, dtype=path.C.dtype).pin_memory()
-    dev_in = dict(path.input_tensors())
-    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step():
-        for n, t in host_in:
-            dev_in[n].copy_(t, non_blocking=True)
-        step()
-        host_out.copy_(path.C, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    for e0, e1 in e2e_ev:
-        flush.fill_(1.0)
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else measure_e2e(path, step, args, dist, dev,
+                                                                      flush, stream)
 
     peaks, peak_src = load_peaks()
     flops = wl.flops()
@@ -349,7 +369,7 @@ def run_mxg(args, wl, ws_world, rank, local):
         b = path.kernel_bytes(gemm_name)
         roofline["hbm_bytes"] = b
         roofline["t_hbm_roofline_ms"] = round(b / (peaks["hbm_gbs"] * 1e9) * 1e3, 5)
-    value = ws_world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, ws_world, ms)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -363,9 +383,11 @@ def run_mxg(args, wl, ws_world, rank, local):
                    "parallelism": "replicas" if ws_world > 1 else "single GPU"},
         "roofline": roofline,
         "kernels": kernels,
-        "e2e": {"value": round(ws_world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_ms is None else {
+            "value": round(job_tflops(flops, ws_world, e2e_ms), 2), "unit": "TFLOP/s",
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "same C-ABI calls; inputs copied from pinned host memory and the output copied "
+                    "back inside each timed step"},
         "gpu_launches": int(launches),
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
@@ -485,11 +507,18 @@ def main():
     ap.add_argument("--out", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--M", type=int, default=0, help="override live rows (profiling runs)")
+    ap.add_argument("--N", type=int, default=0, help="override N (profiling runs)")
+    ap.add_argument("--K", type=int, default=0, help="override K (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "mxg":
         args.warmup = 3
     from moe_grouped_block_gb300 import workloads
     wl = workloads.WORKLOADS[args.config]
+    over = {k: v for k, v in (("M", args.M), ("N", args.N), ("K", args.K)) if v}
+    if over:
+        wl = wl.scaled(name=wl.name + "_reduced", **over)
     ws_world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, wl, ws_world, rank)

@@ -74,7 +74,8 @@ typedef enum { MXG_ROWWISE = 1, MXG_COLWISE = 2, MXG_BOTH = 3 } mxg_qlayout_t;
 
 typedef enum {
   MXG_FPROP_TN = 0, /* ragged output rows:  C[M_cap, N] = X[M_cap, K] . W[g]^T  */
-  MXG_WGRAD_NT = 1  /* ragged contraction:  dW[G, N, K] = dY_g^T . X_g          */
+  MXG_WGRAD_NT = 1, /* ragged contraction:  dW[G, N, K] = dY_g^T . X_g          */
+  MXG_DGRAD_NN = 2  /* ragged output rows:  dX[M_cap, K] = dY[M_cap, N] . W[g]  */
 } mxg_gemm_mode_t;
 
 typedef enum { MXG_OUT_F32 = 0, MXG_OUT_BF16 = 1 } mxg_out_t;
@@ -182,20 +183,49 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *   dW[g, n, k] = alpha_g * sum_{m in group g} A[n, m] * B[k, m]
  *                 + beta_g * dW[g, n, k];   C = dW is [G, N, K].
  *   An empty group writes beta_g * dW[g] (zeros when beta is NULL).
+ * MXG_DGRAD_NN (ragged rows, weights not transposed, MXFP8; [TE-gemm]
+ * _quantize_gemm_operands: an RHS whose contraction dim is not last is
+ * quantized colwise):
+ *   A = rowwise dY: data [M_cap, N], scale [M_cap, N/32];
+ *   B = colwise copy of W viewed as [G*N, K]: data [K, G*N], scale
+ *       [K, G*N/32] (mxg_group_quantize(MXFP8, COLWISE, W, G*N, K, NULL, ...)).
+ *   dX[off_g + i, k] = alpha_g * sum_n A[off_g+i, n] * B[k, g*N + n]
+ *                      + beta_g * dX[off_g + i, k];   C = dX is [M_cap, K].
  * group_ws : offsets workspace of mxg_group_offsets (first G entries used).
  * alpha, beta : device float[G] or NULL (alpha = 1, beta = 0).
+ * bias  : device float [G, N] (fprop) or [G, K] (dgrad), or NULL: per-group
+ *         bias ([TE-gemm] grouped_gemm: bias of shape (G, N)); the output is
+ *         alpha_g * acc + bias[g, col] + beta_g * C.  Rejected for wgrad.
  * workspace : not needed by this implementation (size query returns 0);
  *             may be NULL.
  * Accumulation is FP32 in tensor memory; the FP32 output is the parity
  * output, bf16 is rounded to nearest even from it.
- * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 wgrad, beta with
- * NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
+ * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 wgrad or dgrad, beta
+ * with NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
  * 128; data/scale/C not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
 mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
                               const mxg_operand_t* B, const int64_t* group_ws, int G,
                               int64_t M_cap, int64_t N, int64_t K, const float* alpha,
-                              const float* beta, void* C, mxg_out_t out_type, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_status, mxg_stream_t stream);
+                              const float* beta, const float* bias, void* C, mxg_out_t out_type,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              mxg_stream_t stream);
+
+/* Test hook for the failure path of the GEMM's bounded pipeline waits (no
+ * counterpart on the pages).  Same arguments and checks as mxg_grouped_gemm,
+ * plus:
+ *   inject_flags    : bit 0 -- CTA 0 withholds the arrival that tells its
+ *                     epilogue that its first accumulator is ready, so the
+ *                     epilogue's wait runs out; 0 -- a normal run.
+ *   wait_timeout_ns : bound on every pipeline wait, in ns (0 = 1 s default).
+ * With bit 0 set the launch ends with MXG_DEV_TIMEOUT in dev_status, the
+ * affected CTA drains its copies and MMAs, frees its tensor memory and
+ * returns; the output is undefined and the device stays usable. */
+mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                                    const mxg_operand_t* B, const int64_t* group_ws, int G,
+                                    int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                                    const float* beta, const float* bias, void* C,
+                                    mxg_out_t out_type, int32_t* dev_status, int inject_flags,
+                                    int64_t wait_timeout_ns, mxg_stream_t stream);
 
 /* Workspace bytes mxg_grouped_gemm needs (0 for every combination here). */
 size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,

@@ -4,6 +4,7 @@
 // grouped GEMM; PR #3661 for the row-scaled NVFP4 variant):
 //   fprop TN (ragged rows):        C[off_g+i, n] = alpha_g * sum_k A[off_g+i, k] B[g*N+n, k]
 //   wgrad NT (ragged contraction): dW[g, n, k]   = alpha_g * sum_{m in g} A[n, m] B[k, m]
+//   dgrad NN (ragged rows):        dX[off_g+i, k] = alpha_g * sum_n A[off_g+i, n] B[k, g*N+n]
 // (+ beta_g * previous C), with E4M3 x E8M0/1x32 (MXFP8) or E2M1 x
 // E4M3/1x16 (NVFP4) operands whose scales arrive pre-swizzled from the
 // grouped quantize, FP32 accumulation in tensor memory and an epilogue that
@@ -45,14 +46,19 @@ struct GemmParams {
   const int64_t* group_ws;
   const float* alpha;
   const float* beta;
+  const float* bias;  // [G, out_cols] or null
   void* C;
   int32_t* status;
   int64_t M_cap, N, K;
-  int64_t atoms_row;  // 512-byte scale tiles per 128-row band of an operand
-  int64_t kb_fprop;   // K blocks (128 bytes) of one fprop tile
+  int64_t a_atoms_row;  // 512-byte scale tiles per 128-row band of A
+  int64_t b_atoms_row;  // ... of B
+  int64_t kb_uniform;   // K blocks (128 bytes) of one fprop / dgrad tile
+  int64_t out_cols;     // columns of C (N for fprop, K for dgrad and wgrad)
+  uint64_t timeout_ns;  // bound on every pipeline wait
   int G;
-  int mode;  // 0 fprop, 1 wgrad
+  int mode;  // 0 fprop, 1 wgrad, 2 dgrad
   int out_bf16;
+  int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
 };
 
 template <int BN, int STAGES, int ACC, bool NVF4>
@@ -89,7 +95,8 @@ struct GemmCfg {
 struct TileInfo {
   int g;
   int64_t a_row, b_row;      // first row of the A / B tile (TMA coordinate 1)
-  int64_t kb_begin, kb_end;  // K blocks of 128 bytes
+  int64_t kb_count;          // K blocks (128 bytes) of this tile
+  int64_t a_kb0, b_kb0;      // first K block of A and of B
   int64_t c_row, c_col;      // top-left output element
   int64_t row_end;           // rows of C at or beyond this are not written
 };
@@ -98,7 +105,7 @@ template <int BN>
 __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, const int32_t* row_off,
                                              const int32_t* tile_off) {
   TileInfo ti;
-  if (p.mode == 0) {
+  if (p.mode != 1) {  // fprop / dgrad: ragged output rows
     int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -113,9 +120,12 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     const int64_t n_tile = local / mt, m_tile = local % mt;
     ti.g = g;
     ti.a_row = row_off[g] + 128 * m_tile;
-    ti.b_row = static_cast<int64_t>(g) * p.N + BN * n_tile;
-    ti.kb_begin = 0;
-    ti.kb_end = p.kb_fprop;
+    // fprop: B rows are expert g's weight rows; dgrad: B is the transposed
+    // weight copy [K, G*N] and expert g is its K-slab g*N .. g*N+N-1
+    ti.b_row = p.mode == 0 ? static_cast<int64_t>(g) * p.N + BN * n_tile : BN * n_tile;
+    ti.kb_count = p.kb_uniform;
+    ti.a_kb0 = 0;
+    ti.b_kb0 = p.mode == 0 ? 0 : (static_cast<int64_t>(g) * p.N) >> 7;
     ti.c_row = ti.a_row;
     ti.c_col = BN * n_tile;
     ti.row_end = row_off[g + 1];
@@ -127,8 +137,8 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.g = g;
     ti.a_row = 128 * n_tile;
     ti.b_row = BN * k_tile;
-    ti.kb_begin = row_off[g] >> 7;
-    ti.kb_end = row_off[g + 1] >> 7;
+    ti.kb_count = (row_off[g + 1] - row_off[g]) >> 7;
+    ti.a_kb0 = ti.b_kb0 = row_off[g] >> 7;
     ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
@@ -137,10 +147,11 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
 }
 
 // Bounded wait used only while tearing down: ignores the abort flag.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, int32_t* status,
+                                                uint64_t timeout_ns) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitTimeoutNs) {
+    if (globaltimer() - t0 > timeout_ns) {
       status_set(status, MXG_DEV_TIMEOUT);
       return;
     }
@@ -192,7 +203,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     // group tables: sanitised row offsets and tile offsets (fprop)
     int64_t carry_rows = 0, carry_tiles = 0;
     int32_t bits = 0;
-    const int64_t ntiles_n = p.N / BN;
+    const int64_t ntiles_n = p.out_cols / BN;
     for (int base = 0; base < p.G; base += 32) {
       const int g = base + static_cast<int>(lane);
       int64_t s = 0;
@@ -217,7 +228,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       const int64_t before = min(carry_rows + incl - s, p.M_cap);
       const int64_t after = min(carry_rows + incl, p.M_cap);
       if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
-      const int64_t tiles_g = p.mode == 0 ? ((after - before) >> 7) * ntiles_n : 0;
+      const int64_t tiles_g = p.mode != 1 ? ((after - before) >> 7) * ntiles_n : 0;
       int64_t tincl = tiles_g;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_s;
   const int64_t total_tiles =
-      p.mode == 0 ? static_cast<int64_t>(tile_off[p.G]) : p.G * (p.N >> 7) * (p.K / BN);
+      p.mode != 1 ? static_cast<int64_t>(tile_off[p.G]) : p.G * (p.N >> 7) * (p.K / BN);
 
   // ------------------------------------------------------------ producer
   if (warp == 0) {
@@ -256,8 +267,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
-        for (int64_t kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -267,14 +278,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-          tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(kb * 128), static_cast<int32_t>(ti.a_row));
-          tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kb * 128), static_cast<int32_t>(ti.b_row));
-          const int64_t katom = kb * Cfg::kAtomsK;
-          bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.atoms_row + katom) * 512, Cfg::kSfaBytes, fb);
+          const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
+          tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(ka * 128), static_cast<int32_t>(ti.a_row));
+          tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * 128), static_cast<int32_t>(ti.b_row));
+          bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.a_atoms_row + ka * Cfg::kAtomsK) * 512,
+                    Cfg::kSfaBytes, fb);
 #pragma unroll
           for (int i = 0; i < BN / 128; ++i)
             bulk_load(ssfb + i * 512 * Cfg::kAtomsK,
-                      p.b_sf + (((ti.b_row >> 7) + i) * p.atoms_row + katom) * 512,
+                      p.b_sf + (((ti.b_row >> 7) + i) * p.b_atoms_row + kbb * Cfg::kAtomsK) * 512,
                       512 * Cfg::kAtomsK, fb);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       }
       // every copy this thread issued has landed before the CTA may exit
       for (int s = 0; s < STAGES; ++s)
-        if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u, p.status);
+        if (issued_mask & (1u << s)) mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u, p.status, p.timeout_ns);
     }
   }
   // ------------------------------------------------------------ MMA issuer
@@ -296,11 +308,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) break;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int64_t kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = smem_desc(sa + 32 * kk, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, 1024, 2);
-            const uint32_t accum = (kb > ti.kb_begin || kk > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (NVF4) {
               tc_mma_nvf4(d_tmem, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
                           sfb_t + kk * 4 * (BN / 128), accum);
@@ -344,7 +356,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));  // accumulator ready (immediately if no K blocks)
+        // accumulator ready (immediately if no K blocks); the test hook withholds
+        // this arrival once so that the epilogue's bounded wait runs out
+        if (!((p.inject & 1) && blockIdx.x == 0 && t == blockIdx.x)) tc_commit(tfull_bar(acc));
         if (++acc == ACC) {
           acc = 0;
           acc_phase ^= 1u;
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       }
       // all MMAs this thread issued have completed before TMEM is freed
       tc_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0, p.status);
+      mbar_wait_drain(drain_bar, 0, p.status, p.timeout_ns);
     }
   }
   // ------------------------------------------------------------ epilogue
@@ -363,10 +377,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
-      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status)) break;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
-      const bool has_k = ti.kb_end > ti.kb_begin;
+      const bool has_k = ti.kb_count > 0;
       if (has_k) {
         const uint32_t taddr = tmem_base + ((32u * quarter) << 16) + acc * BN + col0;
 #pragma unroll
@@ -383,12 +397,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
 
       const int64_t row = ti.c_row + 32 * quarter + lane;
       if (row < ti.row_end) {
-        const int64_t ldc = p.mode == 0 ? p.N : p.K;
+        const int64_t ldc = p.out_cols;
         const int64_t cbase = row * ldc + ti.c_col + col0;
         const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
         const float beta = p.beta ? p.beta[ti.g] : 0.0f;
         float rs = 1.0f;
         const float* cs = nullptr;
+        const float* bs = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0
+                                 : nullptr;
         if (NVF4) {
           rs = p.a_outer[row];
           cs = p.b_outer + ti.b_row + col0;
@@ -403,6 +419,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
               float a = has_k ? __uint_as_float(v[c][4 * q4 + e]) : 0.0f;
               if (NVF4) a = a * rs * cs[32 * c + 4 * q4 + e];
               o[e] = alpha * a;
+              if (bs) o[e] += bs[32 * c + 4 * q4 + e];
             }
             const int64_t idx = cbase + 32 * c + 4 * q4;
             if (beta != 0.0f) {
@@ -499,9 +516,12 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* a_outer, const void* b_data, const uint8_t* b_sf,
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
-                                void* C, int out_bf16, int32_t* status, int num_sms, int tile_n,
+                                const float* bias, void* C, int out_bf16, int32_t* status,
+                                int num_sms, int tile_n, int inject, uint64_t timeout_ns,
                                 cudaStream_t stream) {
   GemmParams p;
+  p.inject = inject;
+  p.timeout_ns = timeout_ns;
   p.a_sf = a_sf;
   p.b_sf = b_sf;
   p.a_outer = a_outer;
@@ -509,6 +529,7 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.group_ws = group_ws;
   p.alpha = alpha;
   p.beta = beta;
+  p.bias = bias;
   p.C = C;
   p.status = status;
   p.M_cap = M_cap;
@@ -517,20 +538,28 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.G = G;
   p.mode = mode;
   p.out_bf16 = out_bf16;
-  const int64_t kdim = mode == 0 ? K : M_cap;                 // contraction length
-  p.atoms_row = nvfp4 ? kdim / 64 : kdim / 128;               // (kdim/blk)/4 scale tiles
-  p.kb_fprop = nvfp4 ? K / 256 : K / 128;                     // 128-byte K blocks
-  const int64_t out_cols = mode == 0 ? N : K;
-  const int bn = (tile_n == 128 || out_cols % 256 != 0) ? 128 : 256;
+  // operand geometry: rows x contraction length (elements) of A and B
+  //   fprop: A [M_cap, K], B [G*N, K];  wgrad: A [N, M_cap], B [K, M_cap];
+  //   dgrad: A [M_cap, N], B [K, G*N]  (the transposed weight copy)
+  const int64_t a_rows = mode == 0 ? M_cap : (mode == 1 ? N : M_cap);
+  const int64_t b_rows = mode == 0 ? G * N : K;
+  const int64_t a_kdim = mode == 0 ? K : (mode == 1 ? M_cap : N);
+  const int64_t b_kdim = mode == 0 ? K : (mode == 1 ? M_cap : G * N);
+  const int64_t blk = nvfp4 ? 16 : 32;
+  p.a_atoms_row = a_kdim / blk / 4;
+  p.b_atoms_row = b_kdim / blk / 4;
+  p.kb_uniform = mode == 0 ? (nvfp4 ? K / 256 : K / 128) : (mode == 2 ? N / 128 : 0);
+  p.out_cols = mode == 0 ? N : K;
+  const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
-  const uint64_t kbytes = nvfp4 ? static_cast<uint64_t>(kdim / 2) : static_cast<uint64_t>(kdim);
+  const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2
   CUtensorMap ta, tb;
-  const uint64_t a_rows = mode == 0 ? M_cap : N;
-  const uint64_t b_rows = mode == 0 ? static_cast<uint64_t>(G) * N : K;
-  if (!make_tmap(&ta, a_data, kbytes, a_rows, 128) || !make_tmap(&tb, b_data, kbytes, b_rows, bn))
+  if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128) ||
+      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows, bn))
     return cudaErrorInvalidValue;
 
-  const int64_t max_tiles = mode == 0 ? (M_cap / 128) * (N / bn) : G * (N / 128) * (K / bn);
+  const int64_t max_tiles =
+      mode == 1 ? G * (N / 128) * (K / bn) : (M_cap / 128) * (p.out_cols / bn);
   if (nvfp4) {
     if (bn == 256) return launch_variant<256, 4, 1, true>(ta, tb, p, max_tiles, num_sms, stream);
     return launch_variant<128, 5, 2, true>(ta, tb, p, max_tiles, num_sms, stream);

@@ -26,8 +26,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* a_outer, const void* b_data, const uint8_t* b_sf,
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
-                                void* C, int out_bf16, int32_t* status, int num_sms, int tile_n,
+                                const float* bias, void* C, int out_bf16, int32_t* status,
+                                int num_sms, int tile_n, int inject, uint64_t timeout_ns,
                                 cudaStream_t stream);
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
 namespace {
@@ -140,23 +142,25 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
                   1);
 }
 
-mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
-                              const mxg_operand_t* B, const int64_t* group_ws, int G,
-                              int64_t M_cap, int64_t N, int64_t K, const float* alpha,
-                              const float* beta, void* C, mxg_out_t out_type, void* workspace,
-                              size_t workspace_bytes, int32_t* dev_status, mxg_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
+static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
+                                      const mxg_operand_t* A, const mxg_operand_t* B,
+                                      const int64_t* group_ws, int G, int64_t M_cap, int64_t N,
+                                      int64_t K, const float* alpha, const float* beta,
+                                      const float* bias, void* C, mxg_out_t out_type,
+                                      int32_t* dev_status, int inject,
+                                      uint64_t timeout_ns, mxg_stream_t stream) {
   if (A == nullptr || B == nullptr || C == nullptr || group_ws == nullptr || G < 1 || G > 1024)
     return MXG_ERR_INVALID_ARG;
   if (fmt != MXG_MXFP8_E4M3 && fmt != MXG_NVFP4_ROWSCALED) return MXG_ERR_INVALID_ARG;
-  if (mode != MXG_FPROP_TN && mode != MXG_WGRAD_NT) return MXG_ERR_INVALID_ARG;
+  if (mode != MXG_FPROP_TN && mode != MXG_WGRAD_NT && mode != MXG_DGRAD_NN)
+    return MXG_ERR_INVALID_ARG;
   if (out_type != MXG_OUT_F32 && out_type != MXG_OUT_BF16) return MXG_ERR_INVALID_ARG;
   if (A->data == nullptr || A->scale == nullptr || B->data == nullptr || B->scale == nullptr)
     return MXG_ERR_INVALID_ARG;
   const bool nv = fmt == MXG_NVFP4_ROWSCALED;
   if (nv && (mode != MXG_FPROP_TN || beta != nullptr || A->outer == nullptr || B->outer == nullptr))
     return MXG_ERR_INVALID_ARG;  // row-scaled NVFP4: fprop only, no beta
+  if (bias != nullptr && mode == MXG_WGRAD_NT) return MXG_ERR_INVALID_ARG;
   if (!mult128(M_cap) || !mult128(N) || !mult128(K) || N == 0 || K == 0)
     return MXG_ERR_ALIGNMENT;
   if (nv && (K % 256) != 0) return MXG_ERR_ALIGNMENT;  // one 128-byte K block = 256 E2M1
@@ -169,11 +173,36 @@ mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_
   if (st != MXG_OK) return st;
   if (M_cap == 0) return MXG_OK;
   return launched(mxg::launch_grouped_gemm(
-                      nv, mode == MXG_WGRAD_NT ? 1 : 0, A->data, A->scale, A->outer, B->data,
-                      B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, C,
-                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(),
-                      reinterpret_cast<cudaStream_t>(stream)),
+                      nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
+                      B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
+                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), inject,
+                      timeout_ns, reinterpret_cast<cudaStream_t>(stream)),
                   1);
+}
+
+mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                              const mxg_operand_t* B, const int64_t* group_ws, int G,
+                              int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                              const float* beta, const float* bias, void* C, mxg_out_t out_type,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              mxg_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
+                           out_type, dev_status, 0, mxg::kDefaultWaitNs, stream);
+}
+
+mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                                    const mxg_operand_t* B, const int64_t* group_ws, int G,
+                                    int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                                    const float* beta, const float* bias, void* C,
+                                    mxg_out_t out_type, int32_t* dev_status, int inject_flags,
+                                    int64_t wait_timeout_ns, mxg_stream_t stream) {
+  if (wait_timeout_ns < 0 || (inject_flags & ~1)) return MXG_ERR_INVALID_ARG;
+  const uint64_t t = wait_timeout_ns == 0 ? mxg::kDefaultWaitNs
+                                          : static_cast<uint64_t>(wait_timeout_ns);
+  return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
+                           out_type, dev_status, inject_flags, t, stream);
 }
 
 size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,

@@ -16,8 +16,8 @@
 
 namespace mxg {
 
-// Bound on any single pipeline wait (nanoseconds of %globaltimer).  A wait
-// that runs out sets MXG_DEV_TIMEOUT, raises the CTA's abort flag and
+// Default bound on any single pipeline wait (nanoseconds of %globaltimer).
+// A wait that runs out sets MXG_DEV_TIMEOUT, raises the CTA's abort flag and
 // returns false; no correct pipeline stage takes anywhere near this long.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
 
@@ -72,13 +72,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // kWaitTimeoutNs; on a timeout it records MXG_DEV_TIMEOUT and raises the
 // abort flag.  Returns true when the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((it & 15u) == 15u && globaltimer() - t0 > kWaitTimeoutNs) {
+    if ((it & 15u) == 15u && globaltimer() - t0 > timeout_ns) {
       *abort_flag = 1;
       status_set(status, MXG_DEV_TIMEOUT);
       return false;

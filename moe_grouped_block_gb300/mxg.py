@@ -25,7 +25,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "mxg.h")
 MXG_OK = 0
 MXG_MXFP8_E4M3, MXG_NVFP4_ROWSCALED = 1, 2
 MXG_ROWWISE, MXG_COLWISE, MXG_BOTH = 1, 2, 3
-MXG_FPROP_TN, MXG_WGRAD_NT = 0, 1
+MXG_FPROP_TN, MXG_WGRAD_NT, MXG_DGRAD_NN = 0, 1, 2
 MXG_OUT_F32, MXG_OUT_BF16 = 0, 1
 MXG_DEV_NEG_SIZE, MXG_DEV_MISALIGNED, MXG_DEV_SUM_OVER_CAPACITY = 1, 2, 4
 MXG_DEV_BOUNDS, MXG_DEV_TIMEOUT = 8, 16
@@ -66,7 +66,12 @@ def load() -> ctypes.CDLL:
                                          vp, vp]
         L.mxg_grouped_gemm.restype = c_int
         L.mxg_grouped_gemm.argtypes = [c_int, c_int, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
-                                       vp, c_int, i64, i64, i64, vp, vp, vp, c_int, vp, sz, vp, vp]
+                                       vp, c_int, i64, i64, i64, vp, vp, vp, vp, c_int, vp, sz, vp,
+                                       vp]
+        L.mxg_grouped_gemm_debug.restype = c_int
+        L.mxg_grouped_gemm_debug.argtypes = [c_int, c_int, ctypes.POINTER(Operand),
+                                             ctypes.POINTER(Operand), vp, c_int, i64, i64, i64, vp,
+                                             vp, vp, vp, c_int, vp, c_int, i64, vp]
         L.mxg_grouped_gemm_workspace_bytes.restype = sz
         L.mxg_grouped_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, i64, i64]
         L.mxg_dequantize.restype = c_int
@@ -136,14 +141,29 @@ def mxg_group_quantize(fmt: int, layout: int, x: torch.Tensor, rows_capacity: in
 def mxg_grouped_gemm(fmt: int, mode: int, A: tuple, B: tuple, group_ws: torch.Tensor, G: int,
                      M_cap: int, N: int, K: int, alpha=None, beta=None, C=None,
                      out_type: int = MXG_OUT_F32, workspace=None, workspace_bytes: int = 0,
-                     dev_status=None, stream=None) -> None:
+                     dev_status=None, stream=None, bias=None) -> None:
     """A, B: (data, scale, outer-or-None) device tensors."""
     a = Operand(_p(A[0]), _p(A[1]), _p(A[2]) if len(A) > 2 else None)
     b = Operand(_p(B[0]), _p(B[1]), _p(B[2]) if len(B) > 2 else None)
     _check("mxg_grouped_gemm",
            load().mxg_grouped_gemm(fmt, mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws), G,
-                                   M_cap, N, K, _p(alpha), _p(beta), _p(C), out_type, _p(workspace),
+                                   M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C), out_type,
+                                   _p(workspace),
                                    workspace_bytes, _p(dev_status), _s(stream)))
+
+
+def mxg_grouped_gemm_debug(fmt: int, mode: int, A: tuple, B: tuple, group_ws, G: int, M_cap: int,
+                           N: int, K: int, alpha=None, beta=None, C=None,
+                           out_type: int = MXG_OUT_F32, dev_status=None, inject_flags: int = 0,
+                           wait_timeout_ns: int = 0, stream=None, bias=None) -> None:
+    a = Operand(_p(A[0]), _p(A[1]), _p(A[2]) if len(A) > 2 else None)
+    b = Operand(_p(B[0]), _p(B[1]), _p(B[2]) if len(B) > 2 else None)
+    _check("mxg_grouped_gemm_debug",
+           load().mxg_grouped_gemm_debug(fmt, mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws),
+                                         G, M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C),
+                                         out_type,
+                                         _p(dev_status), inject_flags, wait_timeout_ns,
+                                         _s(stream)))
 
 
 def mxg_grouped_gemm_workspace_bytes(fmt: int, mode: int, G: int, M_cap: int, N: int) -> int:

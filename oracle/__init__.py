@@ -282,7 +282,8 @@ def _per_group(alpha, G):
 
 
 def grouped_gemm_fprop(fmt: str, a: dict, b: dict, group_rows, N: int, K: int,
-                       alpha=None, beta=None, c_in=None, sample_rows=None, sample_cols=None):
+                       alpha=None, beta=None, c_in=None, sample_rows=None, sample_cols=None,
+                       bias=None):
     """fprop TN over ragged row groups.
 
     a: {"q", "sf"[, "outer"]} rowwise-quantized activations [M_cap, K].
@@ -318,6 +319,8 @@ def grouped_gemm_fprop(fmt: str, a: dict, b: dict, group_rows, N: int, K: int,
             acc = acc * np.asarray(a["outer"], np.float64)[ra][:, None]
             acc = acc * np.asarray(b["outer"], np.float64)[rb][None, :]
         res = al[g] * acc
+        if bias is not None:
+            res = res + np.asarray(bias, np.float64)[g][cols][None, :]
         if c_in is not None and be[g] != 0.0:
             res = res + be[g] * np.asarray(c_in, np.float64)[np.ix_(ra, cols)]
         out[sel] = res
@@ -348,3 +351,36 @@ def grouped_gemm_wgrad(a_t: dict, b_t: dict, group_rows, M_cap: int, N: int, K: 
             res = res + be[g] * np.asarray(c_in, np.float64)[g][np.ix_(ns, ks)]
         out[g] = res
     return ns, ks, out
+
+
+def grouped_gemm_dgrad(a: dict, b_t: dict, group_rows, G: int, N: int, K: int, alpha=None,
+                       beta=None, c_in=None, sample_rows=None, sample_cols=None, bias=None):
+    """dgrad NN over ragged row groups (MXFP8), TransformerEngine gemm.py
+    grouped_gemm with the weights not transposed (its _quantize_gemm_operands
+    quantizes such an RHS colwise, i.e. in blocks along N).
+
+    a:   rowwise dY {"q": [M_cap, N], "sf": swizzled [M_cap, N/32]}.
+    b_t: colwise (transposed) copy of W viewed as [G*N, K]:
+         {"q": [K, G*N], "sf": swizzled [K, G*N/32]}.
+    dX[off_g+i, k] = alpha_g * sum_n dq(dY)[off_g+i, n] * dq(W)[g*N+n, k]
+                     (+ beta_g * c_in).  Returns (rows, cols, [rows, cols]).
+    """
+    offs = np.asarray(group_rows, np.int64)
+    al = _per_group(alpha, G)
+    be = np.zeros(G) if beta is None else np.asarray(beta, np.float64).reshape(G)
+    cols = np.arange(K) if sample_cols is None else np.asarray(sample_cols, np.int64)
+    rows = np.arange(offs[-1]) if sample_rows is None else np.asarray(sample_rows, np.int64)
+    WT = dequantize_rows("mxfp8", b_t["q"], b_t["sf"], G * N, cols)  # [len(cols), G*N]
+    out = np.zeros((rows.size, cols.size), np.float64)
+    for g in range(G):
+        sel = np.nonzero((rows >= offs[g]) & (rows < offs[g + 1]))[0]
+        if sel.size == 0:
+            continue
+        A = dequantize_rows("mxfp8", a["q"], a["sf"], N, rows[sel])
+        res = al[g] * (A @ WT[:, g * N:(g + 1) * N].T)
+        if bias is not None:
+            res = res + np.asarray(bias, np.float64)[g][cols][None, :]
+        if c_in is not None and be[g] != 0.0:
+            res = res + be[g] * np.asarray(c_in, np.float64)[np.ix_(rows[sel], cols)]
+        out[sel] = res
+    return rows, cols, out

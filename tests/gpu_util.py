@@ -100,7 +100,7 @@ class tile_n:
 
 
 def fprop_case(wl: workloads.Workload, layout_x=mxg.MXG_ROWWISE, out_type=mxg.MXG_OUT_F32,
-               alpha=None, beta=None, c_in=None, fill_c=0.0):
+               alpha=None, beta=None, c_in=None, fill_c=0.0, bias=None):
     """Quantize x and w and run the fprop GEMM on the GPU.  Returns a dict of
     host inputs, device outputs and the offsets."""
     inp = workloads.make_inputs(wl)
@@ -126,8 +126,9 @@ def fprop_case(wl: workloads.Workload, layout_x=mxg.MXG_ROWWISE, out_type=mxg.MX
         C = torch.full((R, N), fill_c, dtype=cdt, device=DEV)
     al = None if alpha is None else torch.tensor(alpha, dtype=torch.float32, device=DEV)
     be = None if beta is None else torch.tensor(beta, dtype=torch.float32, device=DEV)
+    bi = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(DEV)
     mxg.mxg_grouped_gemm(fmt, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, al, be, C, out_type,
-                         dev_status=st)
+                         dev_status=st, bias=bi)
     torch.cuda.synchronize()
     return {"inp": inp, "ws": ws, "status": st, "qx": qx, "qw": qw, "C": C, "G": G, "N": N,
             "K": K, "R": R}
@@ -154,8 +155,8 @@ def oracle_quantized_operands(wl: workloads.Workload, inp: dict):
 
 
 def oracle_fprop(wl: workloads.Workload, inp: dict, rows=None, cols=None, alpha=None, beta=None,
-                 c_in=None):
+                 c_in=None, bias=None):
     ws, offs, a, b = oracle_quantized_operands(wl, inp)
     r, c, ref = oracle.grouped_gemm_fprop(wl.fmt, a, b, offs, wl.N, wl.K, alpha=alpha, beta=beta,
-                                          c_in=c_in, sample_rows=rows, sample_cols=cols)
+                                          c_in=c_in, sample_rows=rows, sample_cols=cols, bias=bias)
     return offs, r, c, ref, a, b

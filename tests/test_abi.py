@@ -67,20 +67,22 @@ def test_gemm_argument_errors(lib):
     opo = mxg.Operand(FAKE, FAKE, FAKE)
     r = ctypes.byref
     g = L.mxg_grouped_gemm
-    assert g(1, 0, None, r(op), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
-    assert g(1, 0, r(op), r(op), None, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
-    assert g(1, 0, r(op), r(op), FAKE, 0, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
-    assert g(1, 0, r(op), r(op), FAKE, 1025, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
-    assert g(1, 5, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, None, r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), None, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), FAKE, 0, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 0, r(op), r(op), FAKE, 1025, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(1, 5, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
     # NVFP4: wgrad, beta and missing outer scales are rejected
-    assert g(2, 1, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
-    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, FAKE, FAKE, 0, None, 0, None, None) == 1
-    assert g(2, 0, r(op), r(opo), FAKE, 4, 512, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(2, 1, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, FAKE, None, FAKE, 0, None, 0, None, None) == 1
+    assert g(2, 0, r(op), r(opo), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    # bias has no meaning for wgrad
+    assert g(1, 1, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, FAKE, FAKE, 0, None, 0, None, None) == 1
     # alignment
-    assert g(1, 0, r(op), r(op), FAKE, 4, 500, 256, 256, None, None, FAKE, 0, None, 0, None, None) == 2
-    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 200, 256, None, None, FAKE, 0, None, 0, None, None) == 2
-    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 384, None, None, FAKE, 0, None, 0, None, None) == 2
-    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, FAKE + 4, 0, None, 0, None, None) == 2
+    assert g(1, 0, r(op), r(op), FAKE, 4, 500, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 200, 256, None, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 384, None, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(1, 0, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE + 4, 0, None, 0, None, None) == 2
 
 
 def test_dequantize_argument_errors(lib):

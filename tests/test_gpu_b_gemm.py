@@ -36,7 +36,7 @@ def _run_fprop(wl, tn=None, **kw):
     with tile_n(tn):
         case = fprop_case(wl, **kw)
     offs, rows, cols, ref, a, b = oracle_fprop(wl, case["inp"], alpha=kw.get("alpha"),
-                                               beta=kw.get("beta"),
+                                               beta=kw.get("beta"), bias=kw.get("bias"),
                                                c_in=None if kw.get("c_in") is None else
                                                kw["c_in"].double().numpy())
     _assert_operands_match(case, a, b, int(offs[-1]))
@@ -103,6 +103,15 @@ def test_fprop_alpha_beta_and_capacity_padding():
     assert errs.max() <= TOL, errs
     # rows beyond the live count keep their previous contents
     assert np.array_equal(got[wl.M:], c_in.numpy()[wl.M:].astype(np.float64))
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_fprop_per_group_bias(tn):
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=256, N=512)
+    bias = np.random.default_rng(3).standard_normal((wl.G, wl.N)).astype(np.float32)
+    case, offs, rows, ref = _run_fprop(wl, tn, bias=bias, alpha=[0.5] * wl.G)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
 
 
 @pytest.mark.parametrize("tn", [None, 128])
@@ -182,4 +191,40 @@ def test_nvfp4_fprop_alpha():
     alpha = [1.0, -2.0, 0.5, 4.0]
     case, offs, rows, ref = _run_fprop(wl, alpha=alpha)
     errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+# --------------------------------------------------------------------------- dgrad
+@pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (128, 256)])
+def test_dgrad_scaled(tn, K):
+    """dX = dY . W_g: rowwise dY, colwise (transposed) copy of W."""
+    wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=2048, K=K, N=256, G=8)
+    inp = workloads.make_inputs(wl)
+    G, N, M = wl.G, wl.N, wl.M
+    dy_h = workloads.random_bf16((M, N), seed=71, scale=1e-3)
+    ws, st = gpu_offsets(inp["sizes"], N, M)
+    qd, _ = gpu_mxfp8(dy_h.to(DEV), ws, G, mxg.MXG_ROWWISE)
+    w2 = inp["w"].reshape(G * N, K)
+    qwt, _ = gpu_mxfp8(w2.to(DEV), None, G, mxg.MXG_COLWISE)
+    c0 = torch.linspace(-1, 1, M * K).reshape(M, K).float()
+    dX = c0.to(DEV).clone()
+    alpha = [1.0, 0.5, 2.0, -1.0, 1.0, 1.0, 4.0, 0.25]
+    beta = [0.0, 1.0, 0.0, 0.5, 0.0, 2.0, 0.0, 0.0]
+    al = torch.tensor(alpha, dtype=torch.float32, device=DEV)
+    be = torch.tensor(beta, dtype=torch.float32, device=DEV)
+    with tile_n(tn):
+        mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_DGRAD_NN, (qd["q_row"], qd["sf_row"], None),
+                             (qwt["q_col"], qwt["sf_col"], None), ws, G, M, N, K, al, be, dX,
+                             dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rws, _ = oracle.group_offsets(inp["sizes"].numpy(), 1, N, M)
+    offs = oracle.live_rows(rws, G)
+    od = oracle.mxfp8_quantize(dy_h, M, M, rowwise=True)
+    ow = oracle.mxfp8_quantize(w2, G * N, G * N, rowwise=False, colwise=True)
+    assert np.array_equal(qwt["q_col"].cpu().numpy(), ow["q_col"])
+    _, _, ref = oracle.grouped_gemm_dgrad({"q": od["q_row"], "sf": od["sf_row"]},
+                                          {"q": ow["q_col"], "sf": ow["sf_col"]}, offs, G, N, K,
+                                          alpha=alpha, beta=beta, c_in=c0.double().numpy())
+    errs = normwise_errors(dX.cpu().numpy().astype(np.float64), ref, offs)
     assert errs.max() <= TOL, errs

@@ -119,6 +119,9 @@ def test_fprop_beta_and_sampling():
     _, _, C1 = oracle.grouped_gemm_fprop("mxfp8", a, b, offs, N, K, beta=beta, c_in=c_in)
     g_of_row = np.searchsorted(offs, np.arange(M), side="right") - 1
     np.testing.assert_allclose(C1, C0 + beta[g_of_row][:, None] * c_in, rtol=0, atol=1e-15)
+    bias = np.arange(G * N, dtype=np.float64).reshape(G, N) * 0.01
+    _, _, Cb = oracle.grouped_gemm_fprop("mxfp8", a, b, offs, N, K, bias=bias)
+    np.testing.assert_allclose(Cb, C0 + bias[g_of_row], rtol=0, atol=1e-15)
     rows, cols, Cs = oracle.grouped_gemm_fprop("mxfp8", a, b, offs, N, K, sample_rows=[5, 300, 511],
                                                sample_cols=[0, 7, 255])
     assert np.array_equal(Cs, C0[np.ix_([5, 300, 511], [0, 7, 255])])
@@ -189,3 +192,33 @@ def test_nvfp4_post_scale_definition():
     Bf = oracle.dequantize("nvfp4", b["q"], b["sf"], G * N, K, b["outer"])
     ref = Af[256:] @ Bf[N:].T  # summation order differs: compare normwise
     assert np.max(np.abs(C[256:] - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_dgrad_brute_force_and_per_expert():
+    G, N, K, M = 3, 128, 256, 512
+    sizes = [128, 0, 384]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    dy = workloads.random_bf16((M, N), seed=61)
+    w = workloads.random_bf16((G * N, K), seed=62, scale=0.02)
+    qd = oracle.mxfp8_quantize(dy, M, M, rowwise=True)
+    qwt = oracle.mxfp8_quantize(w, G * N, G * N, rowwise=False, colwise=True)
+    alpha = [2.0, 1.0, -0.5]
+    rows, cols, dX = oracle.grouped_gemm_dgrad({"q": qd["q_row"], "sf": qd["sf_row"]},
+                                               {"q": qwt["q_col"], "sf": qwt["sf_col"]}, offs,
+                                               G, N, K, alpha=alpha)
+    A = decode_mxfp8(qd["q_row"], qd["sf_row"], M, N)           # [M, N]
+    WT = decode_mxfp8(qwt["q_col"], qwt["sf_col"], K, G * N)     # [K, G*N]
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        if hi > lo:
+            ref = alpha[g] * (A[lo:hi] @ WT[:, g * N:(g + 1) * N].T)
+            assert np.max(np.abs(dX[lo:hi] - ref)) <= 1e-13 * np.max(np.abs(ref))
+    for (m, k) in [(0, 0), (127, 255), (200, 17), (511, 100)]:
+        g = int(np.searchsorted(offs, m, side="right") - 1)
+        acc = sum(A[m, n] * WT[k, g * N + n] for n in range(N))
+        assert abs(dX[m, k] - alpha[g] * acc) <= 1e-12 * max(1.0, abs(acc))
+    # the colwise weight blocks run along N: each 32-block of a column of W_g
+    # shares one scale, so quantizing W_g^T rowwise gives the same bytes
+    wt = torch.from_numpy(w.float().numpy()[:N].T.copy()).to(torch.bfloat16)
+    qr = oracle.mxfp8_quantize(wt, K, K, rowwise=True)
+    assert np.array_equal(qr["q_row"], qwt["q_col"][:, :N])
