@@ -99,12 +99,18 @@ struct TileInfo {
   int64_t a_kb0, b_kb0;      // first K block of A and of B
   int64_t c_row, c_col;      // top-left output element
   int64_t row_end;           // rows of C at or beyond this are not written
+  bool dup;                  // paired launch: this CTA's half of the pair is past the
+                             // group's last tile (it only helps load the shared B tile)
 };
 
-template <int BN>
+// Work unit t -> tile.  Unpaired: one 128 x BN output tile.  Paired (a
+// 2-CTA cluster): two vertically adjacent tiles sharing one B tile, CTA rank
+// r taking the (2u + r)-th row tile of the unit.
+template <int BN, bool PAIR>
 __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, const int32_t* row_off,
-                                             const int32_t* tile_off) {
+                                             const int32_t* tile_off, uint32_t rank) {
   TileInfo ti;
+  ti.dup = false;
   if (p.mode != 1) {  // fprop / dgrad: ragged output rows
     int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
     while (hi - lo > 1) {
@@ -116,8 +122,14 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     }
     const int g = lo;
     const int64_t mt = (row_off[g + 1] - row_off[g]) >> 7;
+    const int64_t mu = PAIR ? (mt + 1) >> 1 : mt;  // row units per column tile
     const int64_t local = t - tile_off[g];
-    const int64_t n_tile = local / mt, m_tile = local % mt;
+    const int64_t n_tile = local / mu, mu_i = local % mu;
+    int64_t m_tile = PAIR ? 2 * mu_i + rank : mu_i;
+    if (PAIR && m_tile >= mt) {
+      m_tile = 2 * mu_i;
+      ti.dup = true;
+    }
     ti.g = g;
     ti.a_row = row_off[g] + 128 * m_tile;
     // fprop: B rows are expert g's weight rows; dgrad: B is the transposed
@@ -130,10 +142,16 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.c_col = BN * n_tile;
     ti.row_end = row_off[g + 1];
   } else {
-    const int64_t kt = p.K / BN, tpg = (p.N >> 7) * kt;
+    const int64_t nt = p.N >> 7, nu = PAIR ? (nt + 1) >> 1 : nt;
+    const int64_t kt = p.K / BN, tpg = nu * kt;
     const int g = static_cast<int>(t / tpg);
     const int64_t local = t % tpg;
-    const int64_t n_tile = local / kt, k_tile = local % kt;
+    const int64_t nu_i = local / kt, k_tile = local % kt;
+    int64_t n_tile = PAIR ? 2 * nu_i + rank : nu_i;
+    if (PAIR && n_tile >= nt) {
+      n_tile = 2 * nu_i;
+      ti.dup = true;
+    }
     ti.g = g;
     ti.a_row = 128 * n_tile;
     ti.b_row = BN * k_tile;
@@ -158,7 +176,10 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
   }
 }
 
-template <int BN, int STAGES, int ACC, bool NVF4>
+// PAIR: launched as 2-CTA clusters; each CTA loads half of the shared B tile
+// and multicasts it to both, and each MMA issuer releases a stage in both
+// CTAs (a stage is refilled only once both CTAs' MMAs are done with it).
+template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
@@ -185,7 +206,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), PAIR ? 2 : 1);
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -228,7 +249,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       const int64_t before = min(carry_rows + incl - s, p.M_cap);
       const int64_t after = min(carry_rows + incl, p.M_cap);
       if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
-      const int64_t tiles_g = p.mode != 1 ? ((after - before) >> 7) * ntiles_n : 0;
+      const int64_t mt_g = (after - before) >> 7;
+      const int64_t tiles_g = p.mode != 1 ? (PAIR ? (mt_g + 1) >> 1 : mt_g) * ntiles_n : 0;
       int64_t tincl = tiles_g;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -252,10 +274,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the partner's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_s;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int64_t unit0 = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t ustride = PAIR ? (gridDim.x >> 1) : gridDim.x;
+  const int64_t nunits_wgrad = PAIR ? ((p.N >> 7) + 1) >> 1 : (p.N >> 7);
   const int64_t total_tiles =
-      p.mode != 1 ? static_cast<int64_t>(tile_off[p.G]) : p.G * (p.N >> 7) * (p.K / BN);
+      p.mode != 1 ? static_cast<int64_t>(tile_off[p.G]) : p.G * nunits_wgrad * (p.K / BN);
 
   // ------------------------------------------------------------ producer
   if (warp == 0) {
@@ -265,8 +292,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;  // per stage, for the final drain
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+      for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
+        const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
@@ -280,7 +307,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
           const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
           tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(ka * 128), static_cast<int32_t>(ti.a_row));
-          tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * 128), static_cast<int32_t>(ti.b_row));
+          if (PAIR)  // my half of the shared B tile, to both CTAs
+            tma_load_2d_mc(sb + rank * (BN / 2) * 128, &tmap_b, fb, static_cast<int32_t>(kbb * 128),
+                           static_cast<int32_t>(ti.b_row + rank * (BN / 2)), 0x3);
+          else
+            tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * 128),
+                        static_cast<int32_t>(ti.b_row));
           bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.a_atoms_row + ka * Cfg::kAtomsK) * 512,
                     Cfg::kSfaBytes, fb);
 #pragma unroll
@@ -306,8 +338,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+      for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
+        const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -323,6 +355,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
           const uint32_t sfa_t = tmem_base + ACC * BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          if (ti.dup) {  // nothing to compute; release the stage in both CTAs
+            if (PAIR) tc_commit_mc(empty_bar(stage), 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           // scale tiles -> TMEM.  A: tile a at column 4a.  B: for K-step a,
           // band i at column a * 4 * (BN/128) + 4i (the bands of one MMA are
           // adjacent, 4 columns each).
@@ -349,7 +389,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
               tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, accum);
             }
           }
-          tc_commit(empty_bar(stage));  // frees the stage once these MMAs finish
+          // frees the stage (in both CTAs when paired) once these MMAs finish
+          if (PAIR)
+            tc_commit_mc(empty_bar(stage), 0x3);
+          else
+            tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -375,12 +419,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     const uint32_t quarter = warp & 3u;  // TMEM lanes 32*quarter .. +31
     const uint32_t col0 = 128u * (ew >> 2);
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const TileInfo ti = map_tile<BN>(t, p, row_off, tile_off);
+    for (int64_t t = unit0; t < total_tiles; t += ustride) {
+      const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
-      const bool has_k = ti.kb_count > 0;
+      const bool has_k = ti.kb_count > 0 && !ti.dup;
       if (has_k) {
         const uint32_t taddr = tmem_base + ((32u * quarter) << 16) + acc * BN + col0;
 #pragma unroll
@@ -396,7 +440,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       }
 
       const int64_t row = ti.c_row + 32 * quarter + lane;
-      if (row < ti.row_end) {
+      if (!ti.dup && row < ti.row_end) {
         const int64_t ldc = p.out_cols;
         const int64_t cbase = row * ldc + ti.c_col + col0;
         const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
@@ -454,6 +498,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
+  if (PAIR) cluster_sync();  // no multicast or remote arrival targets an exited CTA
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -492,33 +537,55 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int ACC, bool NVF4>
+template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR>
 cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                           int64_t max_tiles, int num_sms, cudaStream_t stream) {
+                           int64_t max_units, int num_sms, cudaStream_t stream) {
   using Cfg = GemmCfg<BN, STAGES, ACC, NVF4>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4, PAIR>;
   const size_t smem = Cfg::smem_bytes(p.G);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
-  if (grid <= 0) return cudaSuccess;
-  kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  if (max_units <= 0) return cudaSuccess;
+  if (!PAIR) {
+    const int grid = static_cast<int>(max_units < num_sms ? max_units : num_sms);
+    kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many co-resident 2-CTA clusters as the device holds (one CTA per SM)
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+    clusters = num_sms / 2;
+  const int64_t n = max_units < clusters ? max_units : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
 }  // namespace
 
 // Tile width: 256 when the output tile dimension allows it (one accumulator
-// stage, 8 epilogue warps), else 128 (two accumulator stages).  The
-// environment variable MXG_GEMM_TILE_N=128 forces the narrow tile.
+// stage, 8 epilogue warps), else 128 (two accumulator stages).  pair = 1
+// launches 2-CTA clusters sharing each B tile by multicast.  The environment
+// variables MXG_GEMM_TILE_N=128 and MXG_GEMM_PAIR=0/1 override the choice.
 cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const uint8_t* a_sf,
                                 const float* a_outer, const void* b_data, const uint8_t* b_sf,
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int inject, uint64_t timeout_ns,
-                                cudaStream_t stream) {
+                                int num_sms, int tile_n, int pair, int inject,
+                                uint64_t timeout_ns, cudaStream_t stream) {
   GemmParams p;
   p.inject = inject;
   p.timeout_ns = timeout_ns;
@@ -552,20 +619,30 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.out_cols = mode == 0 ? N : K;
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
+  const bool pr = pair != 0;
   const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128) ||
-      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows, bn))
+      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows,
+                 pr ? bn / 2 : bn))
     return cudaErrorInvalidValue;
 
-  const int64_t max_tiles =
-      mode == 1 ? G * (N / 128) * (K / bn) : (M_cap / 128) * (p.out_cols / bn);
+  // upper bound on the work units (device-side group sizes are unknown here)
+  int64_t max_units;
+  if (mode == 1)
+    max_units = G * (pr ? ((N / 128) + 1) / 2 : N / 128) * (K / bn);
+  else
+    max_units = (pr ? ((M_cap / 128) + G + 1) / 2 : M_cap / 128) * (p.out_cols / bn);
+#define MXG_LAUNCH(BN_, S_, A_, NV_)                                                   \
+  return pr ? launch_variant<BN_, S_, A_, NV_, true>(ta, tb, p, max_units, num_sms, stream) \
+            : launch_variant<BN_, S_, A_, NV_, false>(ta, tb, p, max_units, num_sms, stream)
   if (nvfp4) {
-    if (bn == 256) return launch_variant<256, 4, 1, true>(ta, tb, p, max_tiles, num_sms, stream);
-    return launch_variant<128, 5, 2, true>(ta, tb, p, max_tiles, num_sms, stream);
+    if (bn == 256) MXG_LAUNCH(256, 4, 1, true);
+    MXG_LAUNCH(128, 5, 2, true);
   }
-  if (bn == 256) return launch_variant<256, 4, 1, false>(ta, tb, p, max_tiles, num_sms, stream);
-  return launch_variant<128, 6, 2, false>(ta, tb, p, max_tiles, num_sms, stream);
+  if (bn == 256) MXG_LAUNCH(256, 4, 1, false);
+  MXG_LAUNCH(128, 6, 2, false);
+#undef MXG_LAUNCH
 }
 
 }  // namespace mxg

@@ -27,8 +27,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int inject, uint64_t timeout_ns,
-                                cudaStream_t stream);
+                                int num_sms, int tile_n, int pair, int inject,
+                                uint64_t timeout_ns, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -77,6 +77,12 @@ mxg_status_t launched(cudaError_t e, uint64_t n) {
 int env_tile_n() {
   const char* s = std::getenv("MXG_GEMM_TILE_N");
   return s ? std::atoi(s) : 0;
+}
+
+// 2-CTA clusters sharing the B tile (default off until enabled here).
+int env_pair() {
+  const char* s = std::getenv("MXG_GEMM_PAIR");
+  return s ? (std::atoi(s) != 0) : 0;
 }
 
 }  // namespace
@@ -175,7 +181,8 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   return launched(mxg::launch_grouped_gemm(
                       nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), inject,
+                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), env_pair(),
+                      inject,
                       timeout_ns, reinterpret_cast<cudaStream_t>(stream)),
                   1);
 }
