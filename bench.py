@@ -450,20 +450,26 @@ def _oracle_sample(wl, rows_per_group: int, cols_per_group: int):
     return time.perf_counter() - t0, flop
 
 
+def _size_sample(wl, budget_s: float):
+    """Grow the per-expert sample (rows = weight rows = side) by doubling
+    until one sample takes at least a quarter of the budget."""
+    side = 128
+    t, f = _oracle_sample(wl, side, side)
+    while t < budget_s / 4 and side < max(wl.N, wl.K):
+        side *= 2
+        t, f = _oracle_sample(wl, side, side)
+    return side, t, f
+
+
 def cpu_baseline(wl, budget_s: float = 15.0):
     import oracle
     oracle.build()
-    cores = os.cpu_count()
-    # calibrate on a small sample, then size the sample to about budget_s
-    t_small, f_small = _oracle_sample(wl, 128, 128)
-    scale = max(1.0, min(64.0, budget_s / max(t_small, 1e-3)))
-    side = int(128 * np.sqrt(scale))
-    t, f = _oracle_sample(wl, side, side)
-    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "seconds": round(t, 2),
-            "sample": "per expert: %d activation rows x %d weight rows, full K=%d, quantize + "
-                      "fp64 GEMM (fprop) / colwise quantize + fp64 GEMM (wgrad)" % (
-                          min(side, wl.M), side, wl.K)}
+    side, t, f = _size_sample(wl, budget_s)
+    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": round(t, 2),
+            "sample": "per expert: up to %d activation rows x %d weight rows (full K=%d): "
+                      "MXFP8/NVFP4 quantize of both operands + fp64 GEMM; throughput = "
+                      "2*rows*cols*K of the sample / its time" % (side, min(side, wl.N), wl.K)}
 
 
 def run_reference(args, wl, ws_world, rank):
@@ -471,10 +477,9 @@ def run_reference(args, wl, ws_world, rank):
         return None
     import oracle
     oracle.build()
-    t_small, f_small = _oracle_sample(wl, 128, 128)
     # each step is a bounded sample; the whole run stays within a few minutes
     per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    side = int(128 * np.sqrt(max(1.0, min(64.0, per_step_budget / max(t_small, 1e-3)))))
+    side, _, _ = _size_sample(wl, per_step_budget)
     for _ in range(args.warmup):
         _oracle_sample(wl, side, side)
     times, flops = [], []

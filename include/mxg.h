@@ -147,7 +147,7 @@ mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int
  *            32x1 blocks along rows
  *   sf_col : E8M0 swizzled [cols, rows_capacity/32] ([TE-gemm]
  *            swizzled_scale, colwise: the scale matrix is transposed first).
- * MXG_NVFP4_ROWSCALED (layout ROWWISE only):
+ * MXG_NVFP4_ROWSCALED, rowwise (layout ROWWISE or BOTH):
  *   q_row     : packed E2M1 [rows_capacity, cols/2]
  *   sf_row    : E4M3 swizzled [rows_capacity, cols/16]
  *   outer_row : FP32 [rows_capacity], s_r = amax_r / 2688
@@ -155,14 +155,24 @@ mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int
  *   Per 1x16 block, fp32 round-to-nearest steps: S = 2688 / amax_r,
  *   sb = E4M3_RNE_satfinite((amax_b / 6) * S), code =
  *   E2M1_RNE_satfinite(x * (S / sb)) (signed zeros when sb or amax_r is 0).
+ * MXG_NVFP4_ROWSCALED, colwise (layout COLWISE or BOTH), written transposed
+ * for wgrad ([PR3661]: columnwise amax per column, split per expert):
+ *   q_col     : packed E2M1 [cols, rows_capacity/2]; byte q_col[k, m/2] holds
+ *               rows m (low nibble) and m+1 of column k
+ *   sf_col    : E4M3 swizzled [cols, rows_capacity/16] (16-row blocks)
+ *   outer_col : FP32 [G, cols] (G = 1 when group_ws is NULL):
+ *               A[g, k] / 2688 with A the amax of column k over group g's
+ *               rows; the same block rule as rowwise runs down the column.
+ *               Groups with no rows get 0.  Requires G <= 1024.
  * Unused output pointers may be NULL.
- * Errors: INVALID_ARG (null required pointer, bad enum, NVFP4 with a colwise
- * layout), ALIGNMENT (rows_capacity or cols not a multiple of 128, pointer
+ * Errors: INVALID_ARG (null required pointer, bad enum, NVFP4 colwise with
+ * G > 1024), ALIGNMENT (rows_capacity or cols not a multiple of 128, pointer
  * not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
 mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const void* x,
                                 int64_t rows_capacity, int64_t cols, const int64_t* group_ws,
                                 int G, void* q_row, uint8_t* sf_row, void* q_col, uint8_t* sf_col,
-                                float* outer_row, int32_t* dev_status, mxg_stream_t stream);
+                                float* outer_row, float* outer_col, int32_t* dev_status,
+                                mxg_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Grouped block-scaled GEMM ([TE-gemm] grouped_gemm; [PR2763] V2 grouped    */
@@ -177,7 +187,10 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *   Rows of C at or beyond the live count are not written.
  *   NVFP4: A.outer [M_cap] and B.outer [G*N] are required, and the result is
  *   multiplied by A.outer[row] * B.outer[g*N + n].
- * MXG_WGRAD_NT (ragged contraction, MXFP8):
+ * MXG_WGRAD_NT (ragged contraction; MXFP8, or row-scaled NVFP4 whose
+ * operands are the colwise copies with A.outer = dY's outer_col [G, N] and
+ * B.outer = X's outer_col [G, K], applied as
+ * dW[g, n, k] *= A.outer[g, n] * B.outer[g, k]):
  *   A = colwise copy of dY: data [N, M_cap], scale [N, M_cap/32];
  *   B = colwise copy of X:  data [K, M_cap], scale [K, M_cap/32].
  *   dW[g, n, k] = alpha_g * sum_{m in group g} A[n, m] * B[k, m]
@@ -200,8 +213,8 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *             may be NULL.
  * Accumulation is FP32 in tensor memory; the FP32 output is the parity
  * output, bf16 is rounded to nearest even from it.
- * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 wgrad or dgrad, beta
- * with NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
+ * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 dgrad, beta with
+ * NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
  * 128; data/scale/C not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
 mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
                               const mxg_operand_t* B, const int64_t* group_ws, int G,

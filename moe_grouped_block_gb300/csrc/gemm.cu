@@ -31,10 +31,8 @@
 //     share one weight tile and the group's activations stay in L2.
 //   * every mbarrier wait is bounded (mbar_wait); after a timeout the CTA
 //     drains its in-flight copies and MMAs, frees TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "mxg_device.cuh"
+#include "mxg_host.h"
 
 namespace mxg {
 
@@ -59,15 +57,23 @@ struct GemmParams {
   int mode;  // 0 fprop, 1 wgrad, 2 dgrad
   int out_bf16;
   int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
+  int prefetch;  // L2 prefetch distance in K blocks (0 = off)
 };
 
-template <int BN, int STAGES, int ACC, bool NVF4>
+// BK: bytes of K per pipeline stage (128 with the 128-byte swizzle, or 64
+// with the 64-byte swizzle: half-size stages, twice as many of them).
+template <int BN, int STAGES, int ACC, bool NVF4, int BK = 128>
 struct GemmCfg {
   static constexpr int kEpiWarps = 4 * (BN / 128);
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
-  static constexpr int kATile = 128 * 128;
-  static constexpr int kBTile = BN * 128;
-  static constexpr int kAtomsK = NVF4 ? 4 : 1;  // scale tiles along K per stage and band
+  static constexpr int kATile = 128 * BK;
+  static constexpr int kBTile = BN * BK;
+  static constexpr int kMmas = BK / 32;          // MMAs (32 bytes of K each) per stage
+  static constexpr int kSwizzle = BK == 128 ? 2 : 4;  // descriptor swizzle mode (128B / 64B)
+  static constexpr int kSbo = 8 * BK;            // bytes between 8-row core-matrix groups
+  // scale tiles along K per stage and band: NVFP4 one per MMA (64 elements);
+  // MXFP8 one 128-element tile, shared by two 64-byte stages when BK = 64
+  static constexpr int kAtomsK = NVF4 ? kMmas : 1;
   static constexpr int kSfaBytes = 512 * kAtomsK;
   static constexpr int kSfbBytes = 512 * kAtomsK * (BN / 128);
   static constexpr int kStageBytes =
@@ -106,7 +112,9 @@ struct TileInfo {
 // Work unit t -> tile.  Unpaired: one 128 x BN output tile.  Paired (a
 // 2-CTA cluster): two vertically adjacent tiles sharing one B tile, CTA rank
 // r taking the (2u + r)-th row tile of the unit.
-template <int BN, bool PAIR>
+// K blocks are BK bytes: BK elements of E4M3, 2*BK of packed E2M1 (EPB =
+// elements per byte).
+template <int BN, bool PAIR, int BK, int EPB>
 __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, const int32_t* row_off,
                                              const int32_t* tile_off, uint32_t rank) {
   TileInfo ti;
@@ -137,7 +145,7 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.b_row = p.mode == 0 ? static_cast<int64_t>(g) * p.N + BN * n_tile : BN * n_tile;
     ti.kb_count = p.kb_uniform;
     ti.a_kb0 = 0;
-    ti.b_kb0 = p.mode == 0 ? 0 : (static_cast<int64_t>(g) * p.N) >> 7;
+    ti.b_kb0 = p.mode == 0 ? 0 : (static_cast<int64_t>(g) * p.N) / (BK * EPB);
     ti.c_row = ti.a_row;
     ti.c_col = BN * n_tile;
     ti.row_end = row_off[g + 1];
@@ -155,8 +163,8 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.g = g;
     ti.a_row = 128 * n_tile;
     ti.b_row = BN * k_tile;
-    ti.kb_count = (row_off[g + 1] - row_off[g]) >> 7;
-    ti.a_kb0 = ti.b_kb0 = row_off[g] >> 7;
+    ti.kb_count = (row_off[g + 1] - row_off[g]) / (BK * EPB);
+    ti.a_kb0 = ti.b_kb0 = row_off[g] / (BK * EPB);
     ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
@@ -179,11 +187,11 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // PAIR: launched as 2-CTA clusters; each CTA loads half of the shared B tile
 // and multicasts it to both, and each MMA issuer releases a stage in both
 // CTAs (a stage is refilled only once both CTAs' MMAs are done with it).
-template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
+template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR, int BK>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4>;
+  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4, BK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -292,8 +300,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;  // per stage, for the final drain
       bool ok = true;
+      // L2 prefetch cursor, p.prefetch K blocks ahead of the loads: the CTAs
+      // that share a B tile walk its K blocks in lockstep, so without it every
+      // stage would wait for a first-touch DRAM read
+      int64_t pf_t = p.prefetch > 0 ? unit0 : total_tiles, pf_kb = p.prefetch;
+      TileInfo pf;
+      pf.kb_count = 0;
+      if (pf_t < total_tiles) pf = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(pf_t, p, row_off, tile_off, rank);
+      auto pf_normalise = [&]() {
+        while (pf_t < total_tiles && pf_kb >= pf.kb_count) {
+          pf_kb -= pf.kb_count;
+          pf_t += ustride;
+          if (pf_t < total_tiles) pf = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(pf_t, p, row_off, tile_off, rank);
+        }
+      };
+      pf_normalise();
       for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
-        const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
+        const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
@@ -306,22 +329,33 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
           const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
-          tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(ka * 128), static_cast<int32_t>(ti.a_row));
+          tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(ka * BK), static_cast<int32_t>(ti.a_row));
           if (PAIR)  // my half of the shared B tile, to both CTAs
-            tma_load_2d_mc(sb + rank * (BN / 2) * 128, &tmap_b, fb, static_cast<int32_t>(kbb * 128),
+            tma_load_2d_mc(sb + rank * (BN / 2) * BK, &tmap_b, fb, static_cast<int32_t>(kbb * BK),
                            static_cast<int32_t>(ti.b_row + rank * (BN / 2)), 0x3);
           else
-            tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * 128),
+            tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * BK),
                         static_cast<int32_t>(ti.b_row));
-          bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.a_atoms_row + ka * Cfg::kAtomsK) * 512,
+          // first scale tile of this stage along K (MXFP8: tiles of 128 bytes of K)
+          const int64_t a_atom = NVF4 ? ka * Cfg::kAtomsK : (ka * BK) >> 7;
+          const int64_t b_atom = NVF4 ? kbb * Cfg::kAtomsK : (kbb * BK) >> 7;
+          bulk_load(ssfa, p.a_sf + ((ti.a_row >> 7) * p.a_atoms_row + a_atom) * 512,
                     Cfg::kSfaBytes, fb);
 #pragma unroll
           for (int i = 0; i < BN / 128; ++i)
             bulk_load(ssfb + i * 512 * Cfg::kAtomsK,
-                      p.b_sf + (((ti.b_row >> 7) + i) * p.b_atoms_row + kbb * Cfg::kAtomsK) * 512,
+                      p.b_sf + (((ti.b_row >> 7) + i) * p.b_atoms_row + b_atom) * 512,
                       512 * Cfg::kAtomsK, fb);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (pf_t < total_tiles) {
+            const int64_t pka = pf.a_kb0 + pf_kb, pkb = pf.b_kb0 + pf_kb;
+            tma_prefetch_2d(&tmap_a, static_cast<int32_t>(pka * BK), static_cast<int32_t>(pf.a_row));
+            tma_prefetch_2d(&tmap_b, static_cast<int32_t>(pkb * BK),
+                            static_cast<int32_t>(pf.b_row + (PAIR ? rank * (BN / 2) : 0)));
+            ++pf_kb;
+            pf_normalise();
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -339,7 +373,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
-        const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
+        const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -376,16 +410,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
               tc_cp_scales(sfb_t + a * 4 * (BN / 128) + 4 * i,
                            smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc(sa + 32 * kk, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, 1024, 2);
+          // MXFP8: byte (K block within the 128-element scale tile) of each MMA
+          const uint32_t sf_id0 = NVF4 ? 0u : static_cast<uint32_t>(((ti.a_kb0 + kb) * BK & 127) >> 5);
+#pragma unroll
+          for (int kk = 0; kk < Cfg::kMmas; ++kk) {
+            const uint64_t adesc = smem_desc(sa + 32 * kk, 16, Cfg::kSbo, Cfg::kSwizzle);
+            const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, Cfg::kSbo, Cfg::kSwizzle);
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (NVF4) {
               tc_mma_nvf4(d_tmem, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
                           sfb_t + kk * 4 * (BN / 128), accum);
             } else {
-              const uint32_t idesc = Cfg::kIdesc | (static_cast<uint32_t>(kk) << 4) |
-                                     (static_cast<uint32_t>(kk) << 29);
+              const uint32_t sid = sf_id0 + kk;
+              const uint32_t idesc = Cfg::kIdesc | (sid << 4) | (sid << 29);
               tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, accum);
             }
           }
@@ -420,7 +457,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
     const uint32_t col0 = 128u * (ew >> 2);
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t t = unit0; t < total_tiles; t += ustride) {
-      const TileInfo ti = map_tile<BN, PAIR>(t, p, row_off, tile_off, rank);
+      const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -449,9 +486,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
         const float* cs = nullptr;
         const float* bs = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0
                                  : nullptr;
-        if (NVF4) {
+        if (NVF4) {  // fprop: per-row / per-weight-row; wgrad: per (group, column) of dY / X
           rs = p.a_outer[row];
-          cs = p.b_outer + ti.b_row + col0;
+          cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -509,39 +546,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4>::kThreads, 1)
 // ---------------------------------------------------------------- host side
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2-D byte tensor [rows, inner_bytes], box [box_rows, 128 bytes], 128-byte
-// swizzle (the layout the K-major MMA descriptors above describe).
+// 2-D byte tensor [rows, inner_bytes], box [box_rows, bk bytes], with the
+// swizzle of the same width (the layout the K-major MMA descriptors above
+// describe).
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows,
-               uint32_t box_rows) {
-  auto enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {inner_bytes, rows};
-  const cuuint64_t strides[1] = {inner_bytes};
-  const cuuint32_t box[2] = {128, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               uint32_t box_rows, int bk) {
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner_bytes, rows, inner_bytes,
+                      static_cast<uint32_t>(bk), box_rows,
+                      bk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR>
+template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR, int BK>
 cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                            int64_t max_units, int num_sms, cudaStream_t stream) {
-  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4, PAIR>;
+  using Cfg = GemmCfg<BN, STAGES, ACC, NVF4, BK>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4, PAIR, BK>;
   const size_t smem = Cfg::smem_bytes(p.G);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -584,9 +603,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int pair, int inject,
-                                uint64_t timeout_ns, cudaStream_t stream) {
+                                int num_sms, int tile_n, int pair, int bk, int prefetch,
+                                int inject, uint64_t timeout_ns, cudaStream_t stream) {
   GemmParams p;
+  p.prefetch = prefetch;
   p.inject = inject;
   p.timeout_ns = timeout_ns;
   p.a_sf = a_sf;
@@ -615,16 +635,22 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   const int64_t blk = nvfp4 ? 16 : 32;
   p.a_atoms_row = a_kdim / blk / 4;
   p.b_atoms_row = b_kdim / blk / 4;
-  p.kb_uniform = mode == 0 ? (nvfp4 ? K / 256 : K / 128) : (mode == 2 ? N / 128 : 0);
+  // bytes of K per pipeline stage; NVFP4 wgrad needs 64 (a 128-row group is
+  // 64 bytes of E2M1 along the contraction)
+  // (and an NVFP4 fprop whose K is not a multiple of 256 elements)
+  const bool need64 = nvfp4 && (mode == 1 || (K % 256) != 0);
+  const int BKB = need64 || (bk == 64 && !pair) ? 64 : 128;
+  if (need64) pair = 0;
+  p.kb_uniform = mode == 0 ? (nvfp4 ? K / 2 : K) / BKB : (mode == 2 ? N / BKB : 0);
   p.out_cols = mode == 0 ? N : K;
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
   const bool pr = pair != 0;
   const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128) ||
+  if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128, BKB) ||
       !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows,
-                 pr ? bn / 2 : bn))
+                 pr ? bn / 2 : bn, BKB))
     return cudaErrorInvalidValue;
 
   // upper bound on the work units (device-side group sizes are unknown here)
@@ -633,9 +659,17 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
     max_units = G * (pr ? ((N / 128) + 1) / 2 : N / 128) * (K / bn);
   else
     max_units = (pr ? ((M_cap / 128) + G + 1) / 2 : M_cap / 128) * (p.out_cols / bn);
-#define MXG_LAUNCH(BN_, S_, A_, NV_)                                                   \
-  return pr ? launch_variant<BN_, S_, A_, NV_, true>(ta, tb, p, max_units, num_sms, stream) \
-            : launch_variant<BN_, S_, A_, NV_, false>(ta, tb, p, max_units, num_sms, stream)
+#define MXG_LAUNCH(BN_, S_, A_, NV_)                                                          \
+  return pr ? launch_variant<BN_, S_, A_, NV_, true, 128>(ta, tb, p, max_units, num_sms, stream) \
+            : launch_variant<BN_, S_, A_, NV_, false, 128>(ta, tb, p, max_units, num_sms, stream)
+  if (BKB == 64) {  // half-size stages, twice as many
+    if (bn == 256) {
+      if (nvfp4) return launch_variant<256, 7, 1, true, false, 64>(ta, tb, p, max_units, num_sms, stream);
+      return launch_variant<256, 8, 1, false, false, 64>(ta, tb, p, max_units, num_sms, stream);
+    }
+    if (nvfp4) return launch_variant<128, 10, 2, true, false, 64>(ta, tb, p, max_units, num_sms, stream);
+    return launch_variant<128, 12, 2, false, false, 64>(ta, tb, p, max_units, num_sms, stream);
+  }
   if (nvfp4) {
     if (bn == 256) MXG_LAUNCH(256, 4, 1, true);
     MXG_LAUNCH(128, 5, 2, true);

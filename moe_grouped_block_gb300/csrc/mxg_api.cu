@@ -19,6 +19,10 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
 cudaError_t launch_nvfp4_quantize(const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q, uint8_t* sf,
                                   float* outer, int32_t* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_nvfp4_quantize_colwise(const uint16_t* x, int64_t cap, int64_t cols,
+                                          const int64_t* group_ws, int G, uint8_t* qT,
+                                          uint8_t* sfT, float* outer, int num_sms,
+                                          cudaStream_t stream);
 cudaError_t launch_dequantize(int nvfp4, int colwise, const uint8_t* q, const uint8_t* sf,
                               const float* outer, int64_t rows, int64_t cols, void* out, int bf16,
                               int num_sms, cudaStream_t stream);
@@ -27,8 +31,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int pair, int inject,
-                                uint64_t timeout_ns, cudaStream_t stream);
+                                int num_sms, int tile_n, int pair, int bk, int prefetch,
+                                int inject, uint64_t timeout_ns, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -79,6 +83,19 @@ int env_tile_n() {
   return s ? std::atoi(s) : 0;
 }
 
+// Bytes of K per GEMM pipeline stage: 128 (default) or 64.
+int env_bk() {
+  const char* s = std::getenv("MXG_GEMM_BK");
+  return s ? std::atoi(s) : 128;
+}
+
+// L2 prefetch distance of the GEMM producer, in K blocks (default off: on
+// GB300 the extra copy instructions cost more than the latency they hide).
+int env_prefetch() {
+  const char* s = std::getenv("MXG_GEMM_PREFETCH");
+  return s ? std::atoi(s) : 0;
+}
+
 // 2-CTA clusters sharing the B tile (default off until enabled here).
 int env_pair() {
   const char* s = std::getenv("MXG_GEMM_PAIR");
@@ -111,7 +128,8 @@ mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int
 mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const void* x,
                                 int64_t rows_capacity, int64_t cols, const int64_t* group_ws,
                                 int G, void* q_row, uint8_t* sf_row, void* q_col, uint8_t* sf_col,
-                                float* outer_row, int32_t* dev_status, mxg_stream_t stream) {
+                                float* outer_row, float* outer_col, int32_t* dev_status,
+                                mxg_stream_t stream) {
   if (x == nullptr || (group_ws != nullptr && (G < 1 || G > 65536))) return MXG_ERR_INVALID_ARG;
   if (layout != MXG_ROWWISE && layout != MXG_COLWISE && layout != MXG_BOTH)
     return MXG_ERR_INVALID_ARG;
@@ -121,7 +139,9 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
         (col && (q_col == nullptr || sf_col == nullptr)))
       return MXG_ERR_INVALID_ARG;
   } else if (fmt == MXG_NVFP4_ROWSCALED) {
-    if (layout != MXG_ROWWISE || q_row == nullptr || sf_row == nullptr || outer_row == nullptr)
+    if ((row && (q_row == nullptr || sf_row == nullptr || outer_row == nullptr)) ||
+        (col && (q_col == nullptr || sf_col == nullptr || outer_col == nullptr)) ||
+        (col && group_ws != nullptr && G > 1024))
       return MXG_ERR_INVALID_ARG;
   } else {
     return MXG_ERR_INVALID_ARG;
@@ -142,10 +162,19 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
                                                static_cast<uint8_t*>(q_col), sf_col, dev_status,
                                                sms, s),
                     1);
-  return launched(mxg::launch_nvfp4_quantize(static_cast<const uint16_t*>(x), rows_capacity, cols,
-                                             group_ws, G, static_cast<uint8_t*>(q_row), sf_row,
-                                             outer_row, dev_status, sms, s),
-                  1);
+  if (row) {
+    const mxg_status_t r = launched(
+        mxg::launch_nvfp4_quantize(static_cast<const uint16_t*>(x), rows_capacity, cols, group_ws,
+                                   G, static_cast<uint8_t*>(q_row), sf_row, outer_row, dev_status,
+                                   sms, s),
+        1);
+    if (r != MXG_OK || !col) return r;
+  }
+  return launched(mxg::launch_nvfp4_quantize_colwise(static_cast<const uint16_t*>(x), rows_capacity,
+                                                     cols, group_ws, G,
+                                                     static_cast<uint8_t*>(q_col), sf_col,
+                                                     outer_col, sms, s),
+                  4);
 }
 
 static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
@@ -164,12 +193,12 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   if (A->data == nullptr || A->scale == nullptr || B->data == nullptr || B->scale == nullptr)
     return MXG_ERR_INVALID_ARG;
   const bool nv = fmt == MXG_NVFP4_ROWSCALED;
-  if (nv && (mode != MXG_FPROP_TN || beta != nullptr || A->outer == nullptr || B->outer == nullptr))
-    return MXG_ERR_INVALID_ARG;  // row-scaled NVFP4: fprop only, no beta
+  if (nv && (mode == MXG_DGRAD_NN || beta != nullptr || A->outer == nullptr || B->outer == nullptr))
+    return MXG_ERR_INVALID_ARG;  // row-scaled NVFP4: fprop and wgrad, no beta
   if (bias != nullptr && mode == MXG_WGRAD_NT) return MXG_ERR_INVALID_ARG;
   if (!mult128(M_cap) || !mult128(N) || !mult128(K) || N == 0 || K == 0)
     return MXG_ERR_ALIGNMENT;
-  if (nv && (K % 256) != 0) return MXG_ERR_ALIGNMENT;  // one 128-byte K block = 256 E2M1
+
   if (M_cap > 0x7FFFFF80LL || N * static_cast<int64_t>(G) > 0x7FFFFF80LL) return MXG_ERR_INVALID_ARG;
   if (!aligned16(A->data) || !aligned16(A->scale) || !aligned16(B->data) || !aligned16(B->scale) ||
       !aligned16(C))
@@ -182,7 +211,7 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
                       nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
                       out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), env_pair(),
-                      inject,
+                      env_bk(), env_prefetch(), inject,
                       timeout_ns, reinterpret_cast<cudaStream_t>(stream)),
                   1);
 }

@@ -13,28 +13,25 @@
 // scales are exactly one 512-byte swizzle tile of sf_row, and its colwise
 // scales exactly one 512-byte tile of sf_col, so both are staged in shared
 // memory and written as 16-byte stores.
-//   phase 1: each half-warp reads one row segment (16 lanes x 16 bytes),
-//            a 4-lane shuffle gives the 1x32 block amax, and the E4M3 bytes
-//            go straight out (8 bytes per lane, 128 contiguous per row).
-//            For the colwise copy the bf16 words are also kept in shared
-//            memory (row-major; 16-byte stores are conflict-free per phase).
-//   phase 2: thread (column pair, 32-row block) reads 32 words down the
-//            tile (a warp reads 32 consecutive words per row: no bank
-//            conflicts), forms the 32x1 block amax of both columns and
-//            writes 32 contiguous bytes of each transposed row.
+//   load:    one thread issues a TMA copy of the CTA's next tile into the
+//            second of two shared-memory buffers while all threads work on
+//            the current one, so a tile's HBM latency overlaps the previous
+//            tile's arithmetic and stores.
+//   phase 1: each half-warp reads one row segment (16 lanes x 16 bytes,
+//            conflict-free per 8-lane phase), a 4-lane shuffle gives the 1x32
+//            block amax, and the E4M3 bytes go straight out (8 bytes per
+//            lane, 128 contiguous per row).
+//   phase 2: thread (column pair, 32-row block) walks 32 words down the tile
+//            twice (a warp reads 32 consecutive words per row: no bank
+//            conflicts) -- once for the 32x1 block amax of both columns, once
+//            to quantize -- and writes 32 contiguous bytes of each transposed
+//            row.
 #include "mxg_device.cuh"
+#include "mxg_host.h"
 
 namespace mxg {
 
 namespace {
-
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 
 // Live rows = sum of the group sizes in the offsets workspace, each taken
 // as non-negative and 128-aligned, clamped to the capacity.  Called by warp
@@ -88,88 +85,119 @@ __device__ __forceinline__ float amax8(const uint4 v) {
 
 }  // namespace
 
+// Shared memory: two 32 KB bf16 tiles (TMA double buffer), two 512-byte scale
+// staging tiles, two mbarriers, the live-row count and the abort flag.
+constexpr int kQTileBytes = 128 * 128 * 2;
+constexpr int kQSmemBytes = 2 * kQTileBytes + 2 * 512 + 2 * 8 + 16 + 1024;
+
 template <bool ROW, bool COL>
 __global__ void __launch_bounds__(256, 3)
-    mxfp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
+    mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                           const int64_t* __restrict__ group_ws, int G, uint8_t* __restrict__ q_row,
                           uint8_t* __restrict__ sf_row, uint8_t* __restrict__ q_col,
                           uint8_t* __restrict__ sf_col, int32_t* status) {
-  __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 4];  // bf16 pairs, row-major
-  __shared__ __align__(16) uint8_t sfr_s[512];
-  __shared__ __align__(16) uint8_t sfc_s[512];
-  __shared__ int64_t live_s;
+  extern __shared__ uint8_t qsmem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* sfr_s = sm + 2 * kQTileBytes;
+  uint8_t* sfc_s = sfr_s + 512;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfc_s + 512);
+  int64_t* live_s = reinterpret_cast<int64_t*>(bars + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(live_s + 1);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
   if (warp == 0) {
     const int64_t l = live_rows_warp(group_ws, G, cap, status);
-    if (lane == 0) live_s = l;
+    if (lane == 0) *live_s = l;
   }
   __syncthreads();
   const int64_t kt = cols >> 7;
-  const int64_t tiles = (live_s >> 7) * kt;
+  const int64_t tiles = (*live_s >> 7) * kt;
+
+  // thread 0 issues the TMA load of tile t into buffer b
+  auto issue = [&](int64_t t, int b) {
+    const uint32_t bar = smem_u32(&bars[b]);
+    mbar_arrive_expect_tx(bar, kQTileBytes);
+    tma_load_2d(smem_u32(sm + b * kQTileBytes), &tmap_x, bar, static_cast<int32_t>((t % kt) << 7),
+                static_cast<int32_t>((t / kt) << 7));
+  };
+  if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
+    prefetch_tmap(&tmap_x);
+    issue(blockIdx.x, 0);
+  }
 
   const uint32_t half = lane >> 4;  // which row of the pair
   const uint32_t cl = lane & 15u;   // 16-byte chunk: columns 8*cl .. 8*cl+7
-
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
-    const uint16_t* xt = x + m0 * cols + k0 + 8 * cl;
-
-    // ---- phase 1: rows
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint4 v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t r = (h * 4 + i) * 16 + warp * 2 + half;
-        v[i] = ld_stream16(xt + static_cast<int64_t>(r) * cols);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t r = (h * 4 + i) * 16 + warp * 2 + half;
-        if (COL) reinterpret_cast<uint4*>(tile)[r * 16 + cl] = v[i];
-        if (ROW) {
-          float a = amax8(v[i]);
-          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-          a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-          const int e = mx_exponent(a);
-          const uint2 o = quant8(v[i], pow2_neg(e));
-          *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
-          if ((cl & 3u) == 0) sfr_s[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] =
-              static_cast<uint8_t>(e + 127);
-        }
-      }
+  uint32_t parity = 0u;  // bit b: phase parity of buffer b
+  uint32_t pending = static_cast<int64_t>(blockIdx.x) < tiles ? 1u : 0u;  // thread 0's loads
+  int b = 0;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, b ^= 1) {
+    // the other buffer was released by the __syncthreads ending the previous tile
+    if (threadIdx.x == 0 && t + gridDim.x < tiles) {
+      issue(t + gridDim.x, b ^ 1);
+      pending |= 1u << (b ^ 1);
     }
+    if (!mbar_wait(smem_u32(&bars[b]), (parity >> b) & 1u, abort_flag, status)) *abort_flag = 1;
+    parity ^= 1u << b;
+    pending &= ~(1u << b);
     __syncthreads();
-    if (ROW && threadIdx.x < 32) {
-      const int64_t atom = (m0 >> 7) * kt + (k0 >> 7);
-      reinterpret_cast<uint4*>(sf_row + atom * 512)[threadIdx.x] =
-          reinterpret_cast<const uint4*>(sfr_s)[threadIdx.x];
+    if (*abort_flag) break;
+
+    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
+    const uint32_t* tile = reinterpret_cast<const uint32_t*>(sm + b * kQTileBytes);
+
+    // ---- phase 1: rows (16 lanes per row, 16-byte chunks; conflict-free per 8-lane phase)
+    if (ROW) {
+#pragma unroll 4
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t r = i * 16 + warp * 2 + half;
+        const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + cl];
+        float a = amax8(v);
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        const int e = mx_exponent(a);
+        const uint2 o = quant8(v, pow2_neg(e));
+        *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
+        if ((cl & 3u) == 0)
+          sfr_s[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
+      }
     }
 
     // ---- phase 2: columns (transposed output)
     if (COL) {
       const uint32_t cp = threadIdx.x & 63u;  // column pair 2cp, 2cp+1
       const uint32_t j = threadIdx.x >> 6;    // 32-row block
-      uint32_t w[32];
+      // pass A: block amax of both columns; pass B: re-read and quantize
+      // (shared memory is cheap here and no 32-word register array is held)
+      const uint32_t* col = tile + (32 * j) * 64 + cp;
       float alo = 0.f, ahi = 0.f;
-#pragma unroll
+#pragma unroll 8
       for (int i = 0; i < 32; ++i) {
-        w[i] = tile[(32 * j + i) * 64 + cp];
-        alo = fmaxf(alo, fabsf(bf16lo(w[i])));
-        ahi = fmaxf(ahi, fabsf(bf16hi(w[i])));
+        const uint32_t w = col[i * 64];
+        alo = fmaxf(alo, fabsf(bf16lo(w)));
+        ahi = fmaxf(ahi, fabsf(bf16hi(w)));
       }
+      const int elo = mx_exponent(alo), ehi = mx_exponent(ahi);
+      const float slo = pow2_neg(elo), shi = pow2_neg(ehi);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int e = mx_exponent(c ? ahi : alo);
-        const float s = pow2_neg(e);
+        const int e = c ? ehi : elo;
+        const float s = c ? shi : slo;
         uint32_t o[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float f0 = (c ? bf16hi(w[4 * i]) : bf16lo(w[4 * i])) * s;
-          const float f1 = (c ? bf16hi(w[4 * i + 1]) : bf16lo(w[4 * i + 1])) * s;
-          const float f2 = (c ? bf16hi(w[4 * i + 2]) : bf16lo(w[4 * i + 2])) * s;
-          const float f3 = (c ? bf16hi(w[4 * i + 3]) : bf16lo(w[4 * i + 3])) * s;
+          const uint32_t w0 = col[(4 * i) * 64], w1 = col[(4 * i + 1) * 64];
+          const uint32_t w2 = col[(4 * i + 2) * 64], w3 = col[(4 * i + 3) * 64];
+          const float f0 = (c ? bf16hi(w0) : bf16lo(w0)) * s;
+          const float f1 = (c ? bf16hi(w1) : bf16lo(w1)) * s;
+          const float f2 = (c ? bf16hi(w2) : bf16lo(w2)) * s;
+          const float f3 = (c ? bf16hi(w3) : bf16lo(w3)) * s;
           o[i] = cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16);
         }
         const uint32_t kk = 2 * cp + c;
@@ -178,15 +206,29 @@ __global__ void __launch_bounds__(256, 3)
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         sfc_s[(kk & 31u) * 16 + (kk >> 5) * 4 + j] = static_cast<uint8_t>(e + 127);
       }
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const int64_t atom = (k0 >> 7) * (cap >> 7) + (m0 >> 7);
-        reinterpret_cast<uint4*>(sf_col + atom * 512)[threadIdx.x] =
-            reinterpret_cast<const uint4*>(sfc_s)[threadIdx.x];
-      }
     }
-    __syncthreads();  // shared buffers are reused by the next tile
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      if (ROW) {
+        const int64_t atom = (m0 >> 7) * kt + (k0 >> 7);
+        reinterpret_cast<uint4*>(sf_row + atom * 512)[threadIdx.x] =
+            reinterpret_cast<const uint4*>(sfr_s)[threadIdx.x];
+      }
+    } else if (COL && threadIdx.x < 64) {
+      const int64_t atom = (k0 >> 7) * (cap >> 7) + (m0 >> 7);
+      reinterpret_cast<uint4*>(sf_col + atom * 512)[threadIdx.x - 32] =
+          reinterpret_cast<const uint4*>(sfc_s)[threadIdx.x - 32];
+    }
+    __syncthreads();  // tile buffer and scale staging are reused
   }
+  // a prefetch still in flight (only after an abort) lands before the CTA exits
+  if (threadIdx.x == 0)
+    for (int bb = 0; bb < 2; ++bb)
+      if (pending & (1u << bb)) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&bars[bb]), (parity >> bb) & 1u))
+          if (globaltimer() - t0 > kWaitTimeoutNs) break;
+      }
 }
 
 cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t cap, int64_t cols,
@@ -195,18 +237,24 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
                                   cudaStream_t stream) {
   const int64_t max_tiles = (cap >> 7) * (cols >> 7);
   if (max_tiles == 0) return cudaSuccess;
-  const int64_t per_sm = col ? 3 : 6;
+  CUtensorMap tm;
+  if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, static_cast<uint64_t>(cols),
+                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const int64_t per_sm = 3;
   const int grid = static_cast<int>(max_tiles < num_sms * per_sm ? max_tiles : num_sms * per_sm);
-  if (row && col)
-    mxfp8_quantize_kernel<true, true><<<grid, 256, 0, stream>>>(x, cap, cols, group_ws, G, q_row,
-                                                                 sf_row, q_col, sf_col, status);
-  else if (row)
-    mxfp8_quantize_kernel<true, false><<<grid, 256, 0, stream>>>(x, cap, cols, group_ws, G, q_row,
-                                                                  sf_row, q_col, sf_col, status);
-  else
-    mxfp8_quantize_kernel<false, true><<<grid, 256, 0, stream>>>(x, cap, cols, group_ws, G, q_row,
-                                                                  sf_row, q_col, sf_col, status);
-  return cudaGetLastError();
+  auto launch = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kQSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 256, kQSmemBytes, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col,
+                                              sf_col, status);
+    return cudaGetLastError();
+  };
+  if (row && col) return launch(mxfp8_quantize_kernel<true, true>);
+  if (row) return launch(mxfp8_quantize_kernel<true, false>);
+  return launch(mxfp8_quantize_kernel<false, true>);
 }
 
 }  // namespace mxg

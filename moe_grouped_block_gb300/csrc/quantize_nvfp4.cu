@@ -16,6 +16,8 @@
 // lane, writes 8 packed bytes per lane (256 contiguous bytes per warp step)
 // and gathers each run of 4 scale bytes -- which are contiguous in the
 // swizzled layout -- into one 32-bit store.
+#include <algorithm>
+
 #include "mxg_device.cuh"
 
 namespace mxg {
@@ -100,10 +102,18 @@ __global__ void __launch_bounds__(256)
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + warp; r < live;
        r += static_cast<int64_t>(gridDim.x) * 8) {
     const uint16_t* xr = x + r * cols;
-    // pass 1: row amax
+    // pass 1: row amax, 8 independent 16-byte loads in flight per lane; the
+    // remainder loop covers rows that are not a multiple of 2048 elements
     float a = 0.f;
-    for (int64_t c = 8 * lane; c < cols; c += 256)
-      a = fmaxf(a, amax8(*reinterpret_cast<const uint4*>(xr + c)));
+    int64_t c = 8 * lane;
+    for (; c + 7 * 256 < cols; c += 8 * 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const uint4*>(xr + c + u * 256);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a = fmaxf(a, amax8(v[u]));
+    }
+    for (; c < cols; c += 256) a = fmaxf(a, amax8(*reinterpret_cast<const uint4*>(xr + c)));
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
     const bool zero_row = !(a > 0.f);
@@ -146,6 +156,192 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
+}
+
+// ------------------------------------------------------------------------
+// Colwise (transposed) row-scaled NVFP4: the copy wgrad consumes (PR #3661
+// sizes the columnwise amax per column and splits it per expert).  For group
+// g and column k the outer scale is A[g,k] / 2688 with A the column amax over
+// the group's rows; R2 then runs down the column in 16-row blocks.  Output
+// qT[k, m/2] (rows m, m+1 in the low / high nibble), E4M3 scales swizzled
+// over [cols, cap/16], outer [G, cols].
+// Four launches: zero the outer buffer; per-tile column amax folded in with
+// atomicMax (order-independent, so deterministic); quantize; outer = A/2688.
+// ------------------------------------------------------------------------
+
+// Sanitised row offsets of the groups into shared memory (warp 0).
+__device__ __forceinline__ void build_row_offsets(const int64_t* ws, int G, int64_t cap,
+                                                  int64_t* row_off) {
+  const uint32_t lane = lane_id();
+  if (ws == nullptr) {
+    if (lane == 0) {
+      row_off[0] = 0;
+      row_off[1] = cap;
+    }
+    return;
+  }
+  int64_t carry = 0;
+  for (int base = 0; base < G; base += 32) {
+    const int g = base + static_cast<int>(lane);
+    int64_t s = 0;
+    if (g < G) {
+      s = ws[g];
+      s = s < 0 ? 0 : (s & ~static_cast<int64_t>(127));
+      s = s > cap ? cap : s;
+    }
+    int64_t incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= static_cast<uint32_t>(d)) incl += v;
+    }
+    if (g < G) row_off[g] = min(carry + incl - s, cap);
+    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  if (lane == 0) row_off[G] = min(carry, cap);
+}
+
+__device__ __forceinline__ int group_of_row(const int64_t* row_off, int G, int64_t m) {
+  int lo = 0, hi = G;  // largest g with row_off[g] <= m
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (row_off[mid] <= m)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+__global__ void nvfp4_col_zero_kernel(float* __restrict__ outer, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    outer[i] = 0.0f;
+}
+
+// Thread (column pair cp, 32-row quarter j) of a 128 x 128 tile.
+__global__ void __launch_bounds__(256)
+    nvfp4_col_amax_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
+                          const int64_t* __restrict__ ws, int G, float* __restrict__ outer) {
+  extern __shared__ int64_t row_off[];
+  const int Gt = ws ? G : 1;
+  if (threadIdx.x < 32) build_row_offsets(ws, G, cap, row_off);
+  __syncthreads();
+  const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
+  const uint32_t cp = threadIdx.x & 63u, j = threadIdx.x >> 6;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
+    const int g = group_of_row(row_off, Gt, m0);
+    const uint32_t* col = reinterpret_cast<const uint32_t*>(x + (m0 + 32 * j) * cols + k0) + cp;
+    float alo = 0.f, ahi = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t w = col[i * (cols >> 1)];
+      alo = fmaxf(alo, fabsf(bf16lo(w)));
+      ahi = fmaxf(ahi, fabsf(bf16hi(w)));
+    }
+    unsigned int* o = reinterpret_cast<unsigned int*>(outer + static_cast<int64_t>(g) * cols + k0 + 2 * cp);
+    atomicMax(o, __float_as_uint(alo));  // non-negative floats order as their bits
+    atomicMax(o + 1, __float_as_uint(ahi));
+  }
+}
+
+__global__ void __launch_bounds__(256)
+    nvfp4_col_quant_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
+                           const int64_t* __restrict__ ws, int G, const float* __restrict__ amax,
+                           uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT) {
+  extern __shared__ int64_t row_off[];
+  __shared__ __align__(16) uint8_t sf_s[2][512];
+  const int Gt = ws ? G : 1;
+  if (threadIdx.x < 32) build_row_offsets(ws, G, cap, row_off);
+  __syncthreads();
+  const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
+  const uint32_t cp = threadIdx.x & 63u, j = threadIdx.x >> 6;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
+    const int g = group_of_row(row_off, Gt, m0);
+    const uint32_t* col = reinterpret_cast<const uint32_t*>(x + (m0 + 32 * j) * cols + k0) + cp;
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = col[i * (cols >> 1)];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t kk = 2 * cp + c;
+      const float A = amax[static_cast<int64_t>(g) * cols + k0 + kk];
+      const bool zero = !(A > 0.f);
+      const float S = zero ? 0.f : __fdiv_rn(2688.0f, A);
+      uint32_t o[4];
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        float ab = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          ab = fmaxf(ab, fabsf(c ? bf16hi(w[16 * blk + i]) : bf16lo(w[16 * blk + i])));
+        uint32_t sbyte = 0;
+        if (!zero) sbyte = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ab, 6.0f), S), 0.f) & 0x7Fu;
+        const float sbv = ue4m3_value(sbyte);
+        const float ratio = sbv == 0.f ? 0.f : __fdiv_rn(S, sbv);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // byte i: rows 2i (low nibble), 2i+1 of this 8-row run
+            const int r = 16 * blk + 8 * h + 2 * i;
+            const float v0 = c ? bf16hi(w[r]) : bf16lo(w[r]);
+            const float v1 = c ? bf16hi(w[r + 1]) : bf16lo(w[r + 1]);
+            uint32_t byte;
+            if (sbv == 0.f) {
+              byte = (signbit(v0) ? 0x8u : 0u) | (signbit(v1) ? 0x80u : 0u);
+            } else {
+              byte = cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio));
+            }
+            word |= byte << (8 * i);
+          }
+          o[2 * blk + h] = word;
+        }
+        const uint32_t sc = 2 * j + blk;  // scale column within the tile (0..7)
+        sf_s[sc >> 2][(kk & 31u) * 16 + (kk >> 5) * 4 + (sc & 3u)] = static_cast<uint8_t>(sbyte);
+      }
+      *reinterpret_cast<uint4*>(qT + (k0 + kk) * (cap >> 1) + ((m0 + 32 * j) >> 1)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+    if (threadIdx.x < 64) {
+      const uint32_t a = threadIdx.x >> 5, l = threadIdx.x & 31u;
+      const int64_t atom = (k0 >> 7) * (cap >> 6) + (m0 >> 6) + a;
+      reinterpret_cast<uint4*>(sfT + atom * 512)[l] = reinterpret_cast<const uint4*>(sf_s[a])[l];
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void nvfp4_col_finalize_kernel(float* __restrict__ outer, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float A = outer[i];
+    outer[i] = A > 0.f ? __fdiv_rn(A, 2688.0f) : 0.0f;
+  }
+}
+
+cudaError_t launch_nvfp4_quantize_colwise(const uint16_t* x, int64_t cap, int64_t cols,
+                                          const int64_t* group_ws, int G, uint8_t* qT,
+                                          uint8_t* sfT, float* outer, int num_sms,
+                                          cudaStream_t stream) {
+  const int Gt = group_ws ? G : 1;
+  const int64_t n_outer = static_cast<int64_t>(Gt) * cols;
+  const int gz = static_cast<int>(std::min<int64_t>((n_outer + 255) / 256, num_sms * 4));
+  nvfp4_col_zero_kernel<<<gz, 256, 0, stream>>>(outer, n_outer);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || cap == 0) return e;
+  const int64_t max_tiles = (cap >> 7) * (cols >> 7);
+  const int grid = static_cast<int>(std::min<int64_t>(max_tiles, num_sms * 4));
+  const size_t smem = sizeof(int64_t) * (Gt + 1);
+  nvfp4_col_amax_kernel<<<grid, 256, smem, stream>>>(x, cap, cols, group_ws, G, outer);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  nvfp4_col_quant_kernel<<<grid, 256, smem, stream>>>(x, cap, cols, group_ws, G, outer, qT, sfT);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  nvfp4_col_finalize_kernel<<<gz, 256, 0, stream>>>(outer, n_outer);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_nvfp4_quantize(const uint16_t* x, int64_t cap, int64_t cols,

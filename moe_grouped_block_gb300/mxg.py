@@ -63,7 +63,7 @@ def load() -> ctypes.CDLL:
         L.mxg_group_offsets.argtypes = [vp, c_int, c_int, i64, i64, i64, vp, vp, vp]
         L.mxg_group_quantize.restype = c_int
         L.mxg_group_quantize.argtypes = [c_int, c_int, vp, i64, i64, vp, c_int, vp, vp, vp, vp, vp,
-                                         vp, vp]
+                                         vp, vp, vp]
         L.mxg_grouped_gemm.restype = c_int
         L.mxg_grouped_gemm.argtypes = [c_int, c_int, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
                                        vp, c_int, i64, i64, i64, vp, vp, vp, vp, c_int, vp, sz, vp,
@@ -130,12 +130,13 @@ def mxg_group_offsets(sizes: torch.Tensor, multiplier: int, last_dim: int, rows_
 
 def mxg_group_quantize(fmt: int, layout: int, x: torch.Tensor, rows_capacity: int, cols: int,
                        group_ws: torch.Tensor | None, G: int, q_row=None, sf_row=None, q_col=None,
-                       sf_col=None, outer_row=None, dev_status=None, stream=None) -> None:
+                       sf_col=None, outer_row=None, dev_status=None, stream=None,
+                       outer_col=None) -> None:
     assert x.dtype == torch.bfloat16 and x.is_contiguous()
     _check("mxg_group_quantize",
            load().mxg_group_quantize(fmt, layout, _p(x), rows_capacity, cols, _p(group_ws), G,
                                      _p(q_row), _p(sf_row), _p(q_col), _p(sf_col), _p(outer_row),
-                                     _p(dev_status), _s(stream)))
+                                     _p(outer_col), _p(dev_status), _s(stream)))
 
 
 def mxg_grouped_gemm(fmt: int, mode: int, A: tuple, B: tuple, group_ws: torch.Tensor, G: int,
@@ -205,7 +206,15 @@ def alloc_mxfp8(rows: int, cols: int, rowwise=True, colwise=False, device="cuda"
     return out
 
 
-def alloc_nvfp4(rows: int, cols: int, device="cuda") -> dict:
-    return {"q_row": torch.empty((rows, cols // 2), dtype=torch.uint8, device=device),
-            "sf_row": torch.empty(rows * cols // 16, dtype=torch.uint8, device=device),
-            "outer_row": torch.empty(rows, dtype=torch.float32, device=device)}
+def alloc_nvfp4(rows: int, cols: int, device="cuda", rowwise=True, colwise=False,
+                G: int = 1) -> dict:
+    out = {}
+    if rowwise:
+        out["q_row"] = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+        out["sf_row"] = torch.empty(rows * cols // 16, dtype=torch.uint8, device=device)
+        out["outer_row"] = torch.empty(rows, dtype=torch.float32, device=device)
+    if colwise:
+        out["q_col"] = torch.empty((cols, rows // 2), dtype=torch.uint8, device=device)
+        out["sf_col"] = torch.empty(rows * cols // 16, dtype=torch.uint8, device=device)
+        out["outer_col"] = torch.empty((G, cols), dtype=torch.float32, device=device)
+    return out

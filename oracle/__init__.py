@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
             L.mxg_oracle_mxfp8_quantize_rowwise.argtypes = [c_p, i64, i64, c_p, c_p]
             L.mxg_oracle_mxfp8_quantize_colwise.argtypes = [c_p, i64, i64, i64, c_p, c_p]
             L.mxg_oracle_nvfp4_quantize_rowwise.argtypes = [c_p, i64, i64, c_p, c_p, c_p]
+            L.mxg_oracle_nvfp4_quantize_colwise.argtypes = [c_p, c_p, ctypes.c_int, i64, i64, c_p,
+                                                            c_p, c_p]
             L.mxg_oracle_mxfp8_dequantize_rows.argtypes = [c_p, c_p, i64, c_p, i64, c_p]
             L.mxg_oracle_nvfp4_dequantize_rows.argtypes = [c_p, c_p, c_p, ctypes.c_int, i64, c_p,
                                                            i64, c_p]
@@ -246,6 +248,23 @@ def nvfp4_quantize(x, rows_live: int, rows_capacity: int, fill: int = 0):
     return {"q_row": q, "sf_row": sf, "outer_row": outer}
 
 
+def nvfp4_quantize_colwise(x, group_rows, rows_capacity: int, fill: int = 0):
+    """Row-scaled NVFP4 (R2) of the columns of each group, written transposed:
+    q_col [cols, rows_cap/2], sf_col swizzled [cols, rows_cap/16], outer_col
+    [G, cols] (per group and column)."""
+    x = _u16(x)
+    R, cols = x.shape
+    offs = np.ascontiguousarray(np.asarray(group_rows, np.int64))
+    G = offs.size - 1
+    assert R == rows_capacity and cols % 128 == 0 and R % 128 == 0
+    qT = np.full((cols, R // 2), fill, np.uint8)
+    sfT = np.full(cols * R // 16, fill, np.uint8)
+    outer = np.full((G, cols), np.nan, np.float32)
+    lib().mxg_oracle_nvfp4_quantize_colwise(_ptr(x), _ptr(offs), G, R, cols, _ptr(qT), _ptr(sfT),
+                                            _ptr(outer))
+    return {"q_col": qT, "sf_col": sfT, "outer_col": outer}
+
+
 # --------------------------------------------------------------------------
 # dequantize
 # --------------------------------------------------------------------------
@@ -328,8 +347,11 @@ def grouped_gemm_fprop(fmt: str, a: dict, b: dict, group_rows, N: int, K: int,
 
 
 def grouped_gemm_wgrad(a_t: dict, b_t: dict, group_rows, M_cap: int, N: int, K: int,
-                       alpha=None, beta=None, c_in=None, sample_n=None, sample_k=None):
-    """wgrad NT over ragged contraction groups (MXFP8).
+                       alpha=None, beta=None, c_in=None, sample_n=None, sample_k=None,
+                       fmt: str = "mxfp8"):
+    """wgrad NT over ragged contraction groups (MXFP8, or row-scaled NVFP4 with
+    per-(group, column) outer scales "outer" [G, N] / [G, K] applied after
+    the neutral-scale product, PR #3661's wgrad).
 
     a_t: colwise (transposed) copy of dY: {"q": [N, M_cap], "sf": [N, M_cap/32] swizzled}.
     b_t: colwise (transposed) copy of X:  {"q": [K, M_cap], "sf": [K, M_cap/32] swizzled}.
@@ -341,12 +363,19 @@ def grouped_gemm_wgrad(a_t: dict, b_t: dict, group_rows, M_cap: int, N: int, K: 
     be = np.zeros(G) if beta is None else np.asarray(beta, np.float64).reshape(G)
     ns = np.arange(N) if sample_n is None else np.asarray(sample_n, np.int64)
     ks = np.arange(K) if sample_k is None else np.asarray(sample_k, np.int64)
-    dYT = dequantize_rows("mxfp8", a_t["q"], a_t["sf"], M_cap, ns)
-    XT = dequantize_rows("mxfp8", b_t["q"], b_t["sf"], M_cap, ks)
+    if fmt == "mxfp8":
+        dYT = dequantize_rows("mxfp8", a_t["q"], a_t["sf"], M_cap, ns)
+        XT = dequantize_rows("mxfp8", b_t["q"], b_t["sf"], M_cap, ks)
+    else:  # neutral outer scales; the per-(group, column) ones come after the product
+        dYT = dequantize_rows("nvfp4", a_t["q"], a_t["sf"], M_cap, ns)
+        XT = dequantize_rows("nvfp4", b_t["q"], b_t["sf"], M_cap, ks)
     out = np.zeros((G, ns.size, ks.size), np.float64)
     for g in range(G):
         lo, hi = offs[g], offs[g + 1]
         res = al[g] * (dYT[:, lo:hi] @ XT[:, lo:hi].T) if hi > lo else np.zeros((ns.size, ks.size))
+        if fmt == "nvfp4":
+            res = res * np.asarray(a_t["outer"], np.float64)[g][ns][:, None]
+            res = res * np.asarray(b_t["outer"], np.float64)[g][ks][None, :]
         if c_in is not None and be[g] != 0.0:
             res = res + be[g] * np.asarray(c_in, np.float64)[g][np.ix_(ns, ks)]
         out[g] = res

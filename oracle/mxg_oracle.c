@@ -383,3 +383,63 @@ ORACLE_API void mxg_oracle_mx_scale_exponent_array(const float* amax, int64_t n,
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; ++i) out[i] = mxg_oracle_mx_scale_exponent(amax[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* R2 applied colwise, written transposed: the columnwise copy PR #3661      */
+/* enables for wgrad, with one amax per column and expert.                  */
+/* Reading taken: for group g and column k the outer scale                  */
+/* is s[g, k] = A / 2688 with A = max over the group's rows of |x[m, k]|;   */
+/* then R2 runs along m over 16-row blocks (groups are 128-row aligned, so  */
+/* blocks never straddle groups).  Output qT[k, m/2] packs rows m (low      */
+/* nibble, even m) and m+1; scales swizzled over [cols, rows_cap/16];      */
+/* outer [G, cols].  group_rows: int64 row offsets [G+1].                   */
+/* ------------------------------------------------------------------------ */
+ORACLE_API void mxg_oracle_nvfp4_quantize_colwise(const uint16_t* x, const int64_t* group_rows,
+                                                  int G, int64_t rows_cap, int64_t cols,
+                                                  uint8_t* qT, uint8_t* sfT, float* outer) {
+  const int64_t C = rows_cap / 16;
+#pragma omp parallel for schedule(static)
+  for (int64_t k = 0; k < cols; ++k) {
+    for (int g = 0; g < G; ++g) {
+      const int64_t lo = group_rows[g], hi = group_rows[g + 1];
+      float A = 0.0f, S, t, sbv, ratio, v;
+      if (hi <= lo) {
+        outer[(int64_t)g * cols + k] = 0.0f;
+        continue;
+      }
+      for (int64_t m = lo; m < hi; ++m) {
+        float a = fabsf(bf16_to_f32(x[m * cols + k]));
+        if (a > A) A = a;
+      }
+      outer[(int64_t)g * cols + k] = A == 0.0f ? 0.0f : A / 2688.0f;
+      S = A == 0.0f ? 0.0f : 2688.0f / A;
+      for (int64_t m0 = lo; m0 < hi; m0 += 16) {
+        float ab = 0.0f;
+        uint8_t sbyte = 0, codes[16];
+        for (int i = 0; i < 16; ++i) {
+          float a = fabsf(bf16_to_f32(x[(m0 + i) * cols + k]));
+          if (a > ab) ab = a;
+        }
+        if (A != 0.0f) {
+          t = ab / 6.0f;
+          t = t * S;
+          sbyte = mxg_oracle_e4m3_encode((double)t) & 0x7F;
+        }
+        sfT[mxg_oracle_swizzle_index(k, m0 / 16, C)] = sbyte;
+        sbv = (float)mxg_oracle_e4m3_decode(sbyte);
+        for (int i = 0; i < 16; ++i) {
+          float xv = bf16_to_f32(x[(m0 + i) * cols + k]);
+          if (sbv == 0.0f) {
+            codes[i] = signbit(xv) ? 0x8 : 0x0;
+          } else {
+            ratio = S / sbv;
+            v = xv * ratio;
+            codes[i] = mxg_oracle_e2m1_encode((double)v);
+          }
+        }
+        for (int i = 0; i < 16; i += 2)
+          qT[k * (rows_cap / 2) + (m0 + i) / 2] = (uint8_t)(codes[i] | (codes[i + 1] << 4));
+      }
+    }
+  }
+}

@@ -35,7 +35,14 @@ def test_scalar_queries(lib):
 
 FAKE = 1 << 20  # a 16-byte-aligned non-null value; never dereferenced (validation fails first)
 
+# The calls below pass fake device pointers that every one of them must
+# reject before any device work.  They are run only where there is no CUDA
+# device, so a validation gap can never turn into a launch.
+no_device_only = pytest.mark.skipif(torch.cuda.is_available(),
+                                    reason="fake-pointer validation tests run without a GPU")
 
+
+@no_device_only
 def test_offsets_argument_errors(lib):
     L = lib
     assert L.mxg_group_offsets(None, 0, 4, 1, 128, 512, FAKE, None, None) == 1
@@ -45,22 +52,24 @@ def test_offsets_argument_errors(lib):
     assert L.mxg_group_offsets(FAKE, 0, 4, 1, 128, -1, None, None, None) == 1
 
 
+@no_device_only
 def test_quantize_argument_errors(lib):
     L = lib
     q = L.mxg_group_quantize
     # bad format / layout
-    assert q(7, 1, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
-    assert q(1, 4, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
+    assert q(7, 1, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 1
+    assert q(1, 4, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 1
     # missing outputs
-    assert q(1, 3, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 1
-    # NVFP4 colwise is not part of the row-scaled path
-    assert q(2, 2, FAKE, 128, 128, None, 1, None, None, FAKE, FAKE, FAKE, None, None) == 1
+    assert q(1, 3, FAKE, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 1
+    # NVFP4 colwise needs its [G, cols] outer-scale output
+    assert q(2, 2, FAKE, 128, 128, None, 1, None, None, FAKE, FAKE, None, None, None, None) == 1
     # sizes not multiples of 128, misaligned pointer
-    assert q(1, 1, FAKE, 100, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
-    assert q(1, 1, FAKE, 128, 96, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
-    assert q(1, 1, FAKE + 8, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None) == 2
+    assert q(1, 1, FAKE, 100, 128, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 2
+    assert q(1, 1, FAKE, 128, 96, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 2
+    assert q(1, 1, FAKE + 8, 128, 128, None, 1, FAKE, FAKE, None, None, None, None, None, None) == 2
 
 
+@no_device_only
 def test_gemm_argument_errors(lib):
     L = lib
     op = mxg.Operand(FAKE, FAKE, None)
@@ -72,8 +81,8 @@ def test_gemm_argument_errors(lib):
     assert g(1, 0, r(op), r(op), FAKE, 0, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
     assert g(1, 0, r(op), r(op), FAKE, 1025, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
     assert g(1, 5, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
-    # NVFP4: wgrad, beta and missing outer scales are rejected
-    assert g(2, 1, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
+    # NVFP4: dgrad, beta and missing outer scales are rejected
+    assert g(2, 2, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
     assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 256, None, FAKE, None, FAKE, 0, None, 0, None, None) == 1
     assert g(2, 0, r(op), r(opo), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 1
     # bias has no meaning for wgrad
@@ -81,10 +90,11 @@ def test_gemm_argument_errors(lib):
     # alignment
     assert g(1, 0, r(op), r(op), FAKE, 4, 500, 256, 256, None, None, None, FAKE, 0, None, 0, None, None) == 2
     assert g(1, 0, r(op), r(op), FAKE, 4, 512, 200, 256, None, None, None, FAKE, 0, None, 0, None, None) == 2
-    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 384, None, None, None, FAKE, 0, None, 0, None, None) == 2
+    assert g(2, 0, r(opo), r(opo), FAKE, 4, 512, 256, 200, None, None, None, FAKE, 0, None, 0, None, None) == 2
     assert g(1, 0, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE + 4, 0, None, 0, None, None) == 2
 
 
+@no_device_only
 def test_dequantize_argument_errors(lib):
     L = lib
     assert L.mxg_dequantize(1, 1, None, FAKE, None, 128, 128, FAKE, 0, None) == 1
@@ -102,3 +112,22 @@ def test_binding_refuses_host_tensors(lib):
     with pytest.raises(ValueError):
         mxg.mxg_group_offsets(torch.zeros(4, dtype=torch.int32), 1, 128, 512,
                               torch.zeros(9, dtype=torch.int64))
+
+
+def test_c_program_compiles_against_the_header(lib, tmp_path):
+    """The plain-C example (run on the GPU by test_gpu_e_c_abi) compiles and
+    links against include/mxg.h and libmxg.so with -Wall -Werror."""
+    import os
+    import shutil
+    import subprocess
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    if shutil.which("gcc") is None or not os.path.exists(os.path.join(cuda, "include")):
+        pytest.skip("needs gcc and the CUDA headers")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run(["gcc", "-O1", "-std=c11", "-Wall", "-Werror",
+                        os.path.join(root, "tests", "c_abi", "c_abi_example.c"),
+                        "-I" + os.path.join(root, "include"), "-I" + os.path.join(cuda, "include"),
+                        "-L" + os.path.dirname(mxg.LIB_PATH), "-lmxg",
+                        "-L" + os.path.join(cuda, "lib64"), "-lcudart",
+                        "-o", str(tmp_path / "c_abi_example")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr

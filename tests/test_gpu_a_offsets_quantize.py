@@ -213,3 +213,32 @@ def test_dequantize_nvfp4():
     got = out.cpu().numpy().astype(np.float64)
     # fp32 product e2m1 * scale * outer: one rounding of the exact fp64 value
     assert np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-38)) <= 2.0 ** -23
+
+
+# --------------------------------------------------------------------------- NVFP4 colwise
+@pytest.mark.parametrize("sizes", [(256, 0, 384, 128, 256), (1024,), (128,) * 8])
+def test_nvfp4_colwise_parity(sizes):
+    G, K = len(sizes), 384
+    live = sum(sizes)
+    R = live + 128  # capacity beyond the live rows
+    x = workloads.random_bf16((R, K), seed=90 + G, dist="student_t3").to(torch.float32)
+    x[:, 7] = 0.0
+    x[:, 9] = -0.0
+    xb = x.to(torch.bfloat16)
+    ws, st = gpu_offsets(torch.tensor(sizes, dtype=torch.int32), K, R)
+    out = mxg.alloc_nvfp4(R, K, device=DEV, rowwise=True, colwise=True, G=G)
+    for k in ("q_col", "sf_col"):
+        out[k].fill_(0x3C)
+    mxg.mxg_group_quantize(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_BOTH, xb.to(DEV), R, K, ws, G,
+                           out["q_row"], out["sf_row"], out["q_col"], out["sf_col"],
+                           out["outer_row"], st, outer_col=out["outer_col"])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    ref = oracle.nvfp4_quantize_colwise(xb, offs, R, fill=0x3C)
+    assert np.array_equal(out["q_col"].cpu().numpy(), ref["q_col"])
+    assert np.array_equal(u8(out["sf_col"]), ref["sf_col"])
+    assert np.array_equal(out["outer_col"].cpu().numpy(), ref["outer_col"])
+    refr = oracle.nvfp4_quantize(xb, live, R)
+    assert np.array_equal(out["q_row"][:live].cpu().numpy(), refr["q_row"][:live])
+    assert np.array_equal(out["outer_row"][:live].cpu().numpy(), refr["outer_row"][:live])

@@ -228,3 +228,43 @@ def test_dgrad_scaled(tn, K):
                                           alpha=alpha, beta=beta, c_in=c0.double().numpy())
     errs = normwise_errors(dX.cpu().numpy().astype(np.float64), ref, offs)
     assert errs.max() <= TOL, errs
+
+
+# --------------------------------------------------------------------------- NVFP4 wgrad
+@pytest.mark.parametrize("K", [512, 384])
+def test_nvfp4_wgrad_scaled(K):
+    """Row-scaled NVFP4 wgrad: colwise copies with per-(group, column) outer
+    scales (PR #3661's wgrad direction)."""
+    wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=2048, K=K, N=256)
+    inp = workloads.make_inputs(wl)
+    G, N, M = wl.G, wl.N, wl.M
+    sizes = inp["sizes"].numpy()
+    ws, st = gpu_offsets(inp["sizes"], K, M)
+    qx = mxg.alloc_nvfp4(M, K, device=DEV, rowwise=False, colwise=True, G=G)
+    qd = mxg.alloc_nvfp4(M, N, device=DEV, rowwise=False, colwise=True, G=G)
+    for q, t, C in ((qx, inp["x"], K), (qd, inp["dy"], N)):
+        mxg.mxg_group_quantize(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_COLWISE, t.to(DEV), M, C, ws, G,
+                               None, None, q["q_col"], q["sf_col"], None, st,
+                               outer_col=q["outer_col"])
+    dW = torch.full((G, N, K), 3.0, dtype=torch.float32, device=DEV)
+    mxg.mxg_grouped_gemm(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_WGRAD_NT,
+                         (qd["q_col"], qd["sf_col"], qd["outer_col"]),
+                         (qx["q_col"], qx["sf_col"], qx["outer_col"]), ws, G, M, N, K, C=dW,
+                         dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    ox = oracle.nvfp4_quantize_colwise(inp["x"], offs, M)
+    od = oracle.nvfp4_quantize_colwise(inp["dy"], offs, M)
+    assert np.array_equal(qx["q_col"].cpu().numpy(), ox["q_col"])
+    assert np.array_equal(qd["outer_col"].cpu().numpy(), od["outer_col"])
+    _, _, ref = oracle.grouped_gemm_wgrad(
+        {"q": od["q_col"], "sf": od["sf_col"], "outer": od["outer_col"]},
+        {"q": ox["q_col"], "sf": ox["sf_col"], "outer": ox["outer_col"]}, offs, M, N, K,
+        fmt="nvfp4")
+    got = dW.cpu().numpy().astype(np.float64)
+    for g in range(G):
+        if sizes[g] == 0:
+            assert not got[g].any()
+        else:
+            assert np.abs(got[g] - ref[g]).max() / np.abs(ref[g]).max() <= TOL, g

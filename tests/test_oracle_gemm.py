@@ -222,3 +222,30 @@ def test_dgrad_brute_force_and_per_expert():
     wt = torch.from_numpy(w.float().numpy()[:N].T.copy()).to(torch.bfloat16)
     qr = oracle.mxfp8_quantize(wt, K, K, rowwise=True)
     assert np.array_equal(qr["q_row"], qwt["q_col"][:, :N])
+
+
+def test_nvfp4_wgrad_brute_force():
+    G, N, K, M = 3, 128, 128, 512
+    offs = np.array([0, 256, 256, 512])
+    x = workloads.random_bf16((M, K), seed=81, dist="student_t3")
+    dy = workloads.random_bf16((M, N), seed=82, scale=1e-3)
+    qx = oracle.nvfp4_quantize_colwise(x, offs, M)
+    qd = oracle.nvfp4_quantize_colwise(dy, offs, M)
+    a = {"q": qd["q_col"], "sf": qd["sf_col"], "outer": qd["outer_col"]}
+    b = {"q": qx["q_col"], "sf": qx["sf_col"], "outer": qx["outer_col"]}
+    ns, ks, dW = oracle.grouped_gemm_wgrad(a, b, offs, M, N, K, fmt="nvfp4")
+    DT = _decode_nvfp4_neutral(qd["q_col"], qd["sf_col"], N, M)   # [N, M]
+    XT = _decode_nvfp4_neutral(qx["q_col"], qx["sf_col"], K, M)   # [K, M]
+    assert not dW[1].any()
+    for (g, n, k) in [(0, 0, 0), (0, 127, 5), (2, 64, 127), (2, 3, 99)]:
+        lo, hi = offs[g], offs[g + 1]
+        acc = sum(DT[n, m] * XT[k, m] for m in range(lo, hi))
+        ref = acc * float(qd["outer_col"][g, n]) * float(qx["outer_col"][g, k])
+        assert abs(dW[g, n, k] - ref) <= 1e-12 * max(abs(ref), 1e-30)
+    # against the full dequantization (outer scale per group and column)
+    for g in (0, 2):
+        lo, hi = offs[g], offs[g + 1]
+        Df = DT[:, lo:hi] * qd["outer_col"][g][:, None].astype(np.float64)
+        Xf = XT[:, lo:hi] * qx["outer_col"][g][:, None].astype(np.float64)
+        ref = Df @ Xf.T
+        assert np.max(np.abs(dW[g] - ref)) <= 1e-12 * np.max(np.abs(ref))

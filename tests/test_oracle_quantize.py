@@ -204,3 +204,35 @@ def test_nvfp4_error_bound_and_nibble_order():
     assert np.all(np.abs(dq - xf) <= blk_amax / 6.0 * 1.1 + 1e-30)
     # relative error is small on average for heavy-tailed rows
     assert np.mean(np.abs(dq - xf)) < 0.2 * np.mean(np.abs(xf))
+
+
+# --------------------------------------------------------------------------- NVFP4 colwise
+def test_nvfp4_colwise_single_group_is_rowwise_of_transpose():
+    x = workloads.random_bf16((256, 384), seed=13, dist="student_t3")
+    col = oracle.nvfp4_quantize_colwise(x, [0, 256], 256)
+    xt = x.t().contiguous()
+    row = oracle.nvfp4_quantize(xt, 384, 384)
+    assert np.array_equal(col["q_col"], row["q_row"])
+    assert np.array_equal(col["sf_col"], row["sf_row"])
+    assert np.array_equal(col["outer_col"][0], row["outer_row"])
+
+
+def test_nvfp4_colwise_groups_brute_force():
+    R, K = 512, 128
+    x = workloads.random_bf16((R, K), seed=14, dist="student_t3").to(torch.float32)
+    x[:, 5] = 0.0          # a zero column in every group
+    x[128:256, 7] = -0.0
+    xb = x.to(torch.bfloat16)
+    offs = [0, 128, 128, 384, 512]  # includes an empty group
+    col = oracle.nvfp4_quantize_colwise(xb, offs, R)
+    sf = page_unswizzle(col["sf_col"], K, R // 16)
+    for g in range(4):
+        lo, hi = offs[g], offs[g + 1]
+        if hi == lo:
+            assert np.all(col["outer_col"][g] == 0.0)
+            continue
+        slab = _f32(xb)[lo:hi].T.copy()  # [K, rows of g]
+        qb, sfb, ob = brute_nvfp4_rowwise(slab)
+        assert np.array_equal(col["q_col"][:, lo // 2:hi // 2], qb)
+        assert np.array_equal(sf[:, lo // 16:hi // 16], sfb)
+        assert np.array_equal(col["outer_col"][g], ob)
