@@ -184,6 +184,127 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
   }
 }
 
+// Group tables in shared memory, built by one warp: sanitised row offsets
+// (sizes clamped at 0, rounded down to 128, the running sum capped at
+// M_cap) and, for fprop / dgrad, each group's first work unit -- a unit is
+// one 128-row tile, or two (pair_units) -- times the column tiles of width bn.
+// CTA 0 records the sanitisation bits in the status word.
+__device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t* row_off,
+                                                   int32_t* tile_off, uint32_t lane,
+                                                   bool pair_units, int bn) {
+  int64_t carry_rows = 0, carry_tiles = 0;
+  int32_t bits = 0;
+  const int64_t ntiles_n = p.out_cols / bn;
+  for (int base = 0; base < p.G; base += 32) {
+    const int g = base + static_cast<int>(lane);
+    int64_t s = 0;
+    if (g < p.G) {
+      s = p.group_ws[g];
+      if (s < 0) {
+        s = 0;
+        bits |= MXG_DEV_NEG_SIZE;
+      }
+      if (s & 127) {
+        s &= ~static_cast<int64_t>(127);
+        bits |= MXG_DEV_MISALIGNED;
+      }
+      if (s > p.M_cap) s = p.M_cap;
+    }
+    int64_t incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+      if (lane >= static_cast<uint32_t>(d)) incl += v;
+    }
+    const int64_t before = min(carry_rows + incl - s, p.M_cap);
+    const int64_t after = min(carry_rows + incl, p.M_cap);
+    if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
+    const int64_t mt_g = (after - before) >> 7;
+    const int64_t tiles_g = p.mode != 1 ? (pair_units ? (mt_g + 1) >> 1 : mt_g) * ntiles_n : 0;
+    int64_t tincl = tiles_g;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, tincl, d);
+      if (lane >= static_cast<uint32_t>(d)) tincl += v;
+    }
+    if (g < p.G) {
+      row_off[g] = static_cast<int32_t>(before);
+      tile_off[g] = static_cast<int32_t>(carry_tiles + tincl - tiles_g);
+    }
+    carry_rows += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    carry_tiles += __shfl_sync(0xFFFFFFFFu, tincl, 31);
+  }
+  if (lane == 0) {
+    row_off[p.G] = static_cast<int32_t>(min(carry_rows, p.M_cap));
+    tile_off[p.G] = static_cast<int32_t>(carry_tiles);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, d);
+  if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
+}
+
+// One output row of the epilogue: 128 accumulator columns (v, four loads of
+// 32) starting at column c_col + col0, with alpha, the NVFP4 outer scales,
+// bias and beta applied, stored as fp32 or bf16.  Rows at or beyond the
+// tile's row_end are skipped.
+template <bool NVF4>
+__device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
+                                             uint32_t col0, const uint32_t (&v)[4][32],
+                                             bool has_k) {
+  if (row >= ti.row_end) return;
+  const int64_t ldc = p.out_cols;
+  const int64_t cbase = row * ldc + ti.c_col + col0;
+  const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
+  const float beta = p.beta ? p.beta[ti.g] : 0.0f;
+  float rs = 1.0f;
+  const float* cs = nullptr;
+  const float* bs =
+      p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0 : nullptr;
+  if (NVF4) {  // fprop: per-row / per-weight-row; wgrad: per (group, column) of dY / X
+    rs = p.a_outer[row];
+    cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+      float o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a = has_k ? __uint_as_float(v[c][4 * q4 + e]) : 0.0f;
+        if (NVF4) a = a * rs * cs[32 * c + 4 * q4 + e];
+        o[e] = alpha * a;
+        if (bs) o[e] += bs[32 * c + 4 * q4 + e];
+      }
+      const int64_t idx = cbase + 32 * c + 4 * q4;
+      if (beta != 0.0f) {
+        if (p.out_bf16) {
+          const uint2 old = *reinterpret_cast<const uint2*>(static_cast<uint16_t*>(p.C) + idx);
+          o[0] += beta * bf16lo(old.x);
+          o[1] += beta * bf16hi(old.x);
+          o[2] += beta * bf16lo(old.y);
+          o[3] += beta * bf16hi(old.y);
+        } else {
+          const float4 old = *reinterpret_cast<const float4*>(static_cast<float*>(p.C) + idx);
+          o[0] += beta * old.x;
+          o[1] += beta * old.y;
+          o[2] += beta * old.z;
+          o[3] += beta * old.w;
+        }
+      }
+      if (p.out_bf16) {
+        uint2 w;
+        w.x = f32_to_bf16_bits(o[0]) | (f32_to_bf16_bits(o[1]) << 16);
+        w.y = f32_to_bf16_bits(o[2]) | (f32_to_bf16_bits(o[3]) << 16);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.C) + idx) = w;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.C) + idx) =
+            make_float4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
 // PAIR: launched as 2-CTA clusters; each CTA loads half of the shared B tile
 // and multicasts it to both, and each MMA issuer releases a stage in both
 // CTAs (a stage is refilled only once both CTAs' MMAs are done with it).
@@ -228,58 +349,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     tmem_alloc(smem_u32(tmem_base_s), Cfg::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 1) {
-    // group tables: sanitised row offsets and tile offsets (fprop)
-    int64_t carry_rows = 0, carry_tiles = 0;
-    int32_t bits = 0;
-    const int64_t ntiles_n = p.out_cols / BN;
-    for (int base = 0; base < p.G; base += 32) {
-      const int g = base + static_cast<int>(lane);
-      int64_t s = 0;
-      if (g < p.G) {
-        s = p.group_ws[g];
-        if (s < 0) {
-          s = 0;
-          bits |= MXG_DEV_NEG_SIZE;
-        }
-        if (s & 127) {
-          s &= ~static_cast<int64_t>(127);
-          bits |= MXG_DEV_MISALIGNED;
-        }
-        if (s > p.M_cap) s = p.M_cap;
-      }
-      int64_t incl = s;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= static_cast<uint32_t>(d)) incl += v;
-      }
-      const int64_t before = min(carry_rows + incl - s, p.M_cap);
-      const int64_t after = min(carry_rows + incl, p.M_cap);
-      if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
-      const int64_t mt_g = (after - before) >> 7;
-      const int64_t tiles_g = p.mode != 1 ? (PAIR ? (mt_g + 1) >> 1 : mt_g) * ntiles_n : 0;
-      int64_t tincl = tiles_g;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int64_t v = __shfl_up_sync(0xFFFFFFFFu, tincl, d);
-        if (lane >= static_cast<uint32_t>(d)) tincl += v;
-      }
-      if (g < p.G) {
-        row_off[g] = static_cast<int32_t>(before);
-        tile_off[g] = static_cast<int32_t>(carry_tiles + tincl - tiles_g);
-      }
-      carry_rows += __shfl_sync(0xFFFFFFFFu, incl, 31);
-      carry_tiles += __shfl_sync(0xFFFFFFFFu, tincl, 31);
-    }
-    if (lane == 0) {
-      row_off[p.G] = static_cast<int32_t>(min(carry_rows, p.M_cap));
-      tile_off[p.G] = static_cast<int32_t>(carry_tiles);
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, d);
-    if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
-  }
+  if (warp == 1) build_group_tables(p, row_off, tile_off, lane, PAIR, BN);
   tc_fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();  // the partner's barriers exist before any multicast
@@ -477,59 +547,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
       }
 
       const int64_t row = ti.c_row + 32 * quarter + lane;
-      if (!ti.dup && row < ti.row_end) {
-        const int64_t ldc = p.out_cols;
-        const int64_t cbase = row * ldc + ti.c_col + col0;
-        const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
-        const float beta = p.beta ? p.beta[ti.g] : 0.0f;
-        float rs = 1.0f;
-        const float* cs = nullptr;
-        const float* bs = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0
-                                 : nullptr;
-        if (NVF4) {  // fprop: per-row / per-weight-row; wgrad: per (group, column) of dY / X
-          rs = p.a_outer[row];
-          cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float a = has_k ? __uint_as_float(v[c][4 * q4 + e]) : 0.0f;
-              if (NVF4) a = a * rs * cs[32 * c + 4 * q4 + e];
-              o[e] = alpha * a;
-              if (bs) o[e] += bs[32 * c + 4 * q4 + e];
-            }
-            const int64_t idx = cbase + 32 * c + 4 * q4;
-            if (beta != 0.0f) {
-              if (p.out_bf16) {
-                const uint2 old = *reinterpret_cast<const uint2*>(static_cast<uint16_t*>(p.C) + idx);
-                o[0] += beta * bf16lo(old.x);
-                o[1] += beta * bf16hi(old.x);
-                o[2] += beta * bf16lo(old.y);
-                o[3] += beta * bf16hi(old.y);
-              } else {
-                const float4 old = *reinterpret_cast<const float4*>(static_cast<float*>(p.C) + idx);
-                o[0] += beta * old.x;
-                o[1] += beta * old.y;
-                o[2] += beta * old.z;
-                o[3] += beta * old.w;
-              }
-            }
-            if (p.out_bf16) {
-              uint2 w;
-              w.x = f32_to_bf16_bits(o[0]) | (f32_to_bf16_bits(o[1]) << 16);
-              w.y = f32_to_bf16_bits(o[2]) | (f32_to_bf16_bits(o[3]) << 16);
-              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.C) + idx) = w;
-            } else {
-              *reinterpret_cast<float4*>(static_cast<float*>(p.C) + idx) =
-                  make_float4(o[0], o[1], o[2], o[3]);
-            }
-          }
-        }
-      }
+      if (!ti.dup) epilogue_row<NVF4>(p, ti, row, col0, v, has_k);
     }
   }
 
@@ -540,6 +558,303 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- CTA-pair kernel
+// A 2-CTA cluster computes one 256 x 256 output unit with the .cta_group::2
+// MMA: the even CTA issues every MMA and scale copy, and each one runs on both
+// SMs.  CTA rank r holds rows 128r..128r+127 of the unit's A tile and of its
+// B tile (the B halves are exchanged by the tensor cores, not copied), the
+// full 256-row B scale tile, and accumulates its 128 x 256 half of the unit
+// in its own tensor memory.  Per SM and pipeline stage that is 32 KB of
+// operands for a 128 x 256 x 128 MMA step, against 48 KB for the single-CTA
+// 128 x 256 tile, and half the MMA instructions.
+template <int STAGES, bool NVF4>
+struct PairCfg {
+  static constexpr int BN = 256, BK = 128;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kATile = 128 * BK;  // this CTA's rows of A
+  static constexpr int kBTile = 128 * BK;  // this CTA's half of B
+  static constexpr int kMmas = BK / 32;
+  static constexpr int kAtomsK = NVF4 ? kMmas : 1;
+  static constexpr int kSfaBytes = 512 * kAtomsK;
+  static constexpr int kSfbBytes = 512 * kAtomsK * 2;
+  static constexpr int kStageBytes =
+      ((kATile + kBTile + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
+  // bytes landing per stage in BOTH CTAs, counted on the even CTA's barrier
+  static constexpr uint32_t kTxBytes = 2u * (kATile + kBTile + kSfaBytes + kSfbBytes);
+  static constexpr int kSfaCols = 4 * kAtomsK;
+  static constexpr int kSfCols = kSfaCols * 3;
+  static constexpr int kTmemCols = 512;
+  static_assert(BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
+  // full[S], empty[S], tfull, tempty, drain; TMEM base; abort flag
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 3) + 16;
+  static size_t smem_bytes(int G) {
+    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 8 * (G + 1) + 16;
+  }
+  // M = 256 (the pair), N = 256; other fields as in GemmCfg
+  static constexpr uint32_t kIdesc = (NVF4 ? ((1u << 7) | (1u << 10)) : 0u) |
+                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (NVF4 ? 0u : (1u << 23)) | ((256u >> 4) << 24);
+};
+
+// Work unit t -> this CTA's half.  fprop / dgrad: 256 rows of one group (the
+// upper half may run past the group's end: it is computed but not stored)
+// times 256 output columns.  wgrad: 256 rows of dW_g times 256 columns.
+// a_row is this CTA's first A row; b_row is the unit's first B row (this CTA
+// loads b_row + 128 * rank).
+template <int EPB>
+__device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p,
+                                                  const int32_t* row_off, const int32_t* tile_off,
+                                                  uint32_t rank) {
+  constexpr int BK = 128;
+  TileInfo ti;
+  ti.dup = false;
+  if (p.mode != 1) {
+    int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_off[mid] <= t)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int g = lo;
+    const int64_t mu = (((row_off[g + 1] - row_off[g]) >> 7) + 1) >> 1;
+    const int64_t local = t - tile_off[g];
+    const int64_t n_tile = local / mu, mu_i = local % mu;
+    ti.g = g;
+    ti.a_row = row_off[g] + 256 * mu_i + 128 * rank;
+    ti.b_row = (p.mode == 0 ? static_cast<int64_t>(g) * p.N : 0) + 256 * n_tile;
+    ti.kb_count = p.kb_uniform;
+    ti.a_kb0 = 0;
+    ti.b_kb0 = p.mode == 0 ? 0 : (static_cast<int64_t>(g) * p.N) / (BK * EPB);
+    ti.c_row = ti.a_row;
+    ti.c_col = 256 * n_tile;
+    ti.row_end = row_off[g + 1];
+  } else {
+    const int64_t nu = ((p.N >> 7) + 1) >> 1, kt = p.K / 256, tpg = nu * kt;
+    const int g = static_cast<int>(t / tpg);
+    const int64_t local = t % tpg;
+    const int64_t nu_i = local / kt, k_tile = local % kt;
+    ti.g = g;
+    ti.a_row = 256 * nu_i + 128 * rank;
+    ti.b_row = 256 * k_tile;
+    ti.kb_count = (row_off[g + 1] - row_off[g]) / (BK * EPB);
+    ti.a_kb0 = ti.b_kb0 = row_off[g] / (BK * EPB);
+    ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
+    ti.c_col = ti.b_row;
+    ti.row_end = static_cast<int64_t>(g + 1) * p.N;
+  }
+  return ti;
+}
+
+template <int STAGES, bool NVF4>
+__global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                             const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ CUtensorMap tmap_sfa,
+                             const __grid_constant__ CUtensorMap tmap_sfb, const GemmParams p) {
+  using Cfg = PairCfg<STAGES, NVF4>;
+  constexpr int BK = Cfg::BK, EPB = NVF4 ? 2 : 1;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
+  int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
+  int32_t* tile_off = row_off + (p.G + 1);
+
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t rank = cluster_ctarank();
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  const uint32_t tfull_bar = smem_u32(&bars[2 * STAGES]);
+  const uint32_t tempty_bar = smem_u32(&bars[2 * STAGES + 1]);
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 2]);
+
+  // ------------------------------------------------------------ set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // even CTA: its producer's arrival + both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // the pair's MMA commit
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * Cfg::kEpiWarps);  // even CTA: both CTAs' epilogue warps
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {  // collective over the pair: both CTAs get the same columns
+    tmem_alloc_pair(smem_u32(tmem_base_s), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 1) build_group_tables(p, row_off, tile_off, lane, true, Cfg::BN);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the even CTA's barriers exist before the odd CTA's copies signal them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_s;
+  const int64_t unit0 = blockIdx.x >> 1;
+  const int64_t ustride = gridDim.x >> 1;
+  const int64_t total_units =
+      p.mode != 1 ? static_cast<int64_t>(tile_off[p.G])
+                  : p.G * ((((p.N >> 7) + 1) >> 1) * (p.K / 256));
+
+  // ------------------------------------------------------------ producers (both CTAs)
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmap_a);
+      prefetch_tmap(&tmap_b);
+      prefetch_tmap(&tmap_sfa);
+      prefetch_tmap(&tmap_sfb);
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_mask = 0, last_parity = 0;
+      bool ok = true;
+      for (int64_t t = unit0; ok && t < total_units; t += ustride) {
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, rank);
+        const int32_t b_half = static_cast<int32_t>(ti.b_row + 128 * rank);
+        const int32_t a_band = static_cast<int32_t>(ti.a_row >> 7);
+        const int32_t b_band = static_cast<int32_t>(ti.b_row >> 7);
+        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sb = sa + Cfg::kATile;
+          const uint32_t ssfa = sb + Cfg::kBTile;
+          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::kTxBytes);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
+          tma_load_2d_pair(sa, &tmap_a, fb, static_cast<int32_t>(ka * BK),
+                           static_cast<int32_t>(ti.a_row));
+          tma_load_2d_pair(sb, &tmap_b, fb, static_cast<int32_t>(kbb * BK), b_half);
+          // scale tiles: this CTA's A band, both B bands of the unit
+          const int64_t a_atom = NVF4 ? ka * Cfg::kAtomsK : ka;
+          const int64_t b_atom = NVF4 ? kbb * Cfg::kAtomsK : kbb;
+          tma_load_2d_pair(ssfa, &tmap_sfa, fb, 0,
+                           static_cast<int32_t>(a_band * p.a_atoms_row + a_atom));
+          tma_load_3d_pair(ssfb, &tmap_sfb, fb, 0, static_cast<int32_t>(b_atom), b_band);
+          issued_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the even CTA's full barriers count both CTAs' bytes: once they have
+      // completed, every copy of the pair has landed
+      if (rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask & (1u << s))
+            mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u, p.status, p.timeout_ns);
+    }
+  }
+  // ------------------------------------------------------------ MMA issuer (even CTA)
+  else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = unit0; ok && t < total_units; t += ustride) {
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, 0);
+        if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        tc_fence_after();
+        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * Cfg::kStageBytes;
+          const uint32_t sb = sa + Cfg::kATile;
+          const uint32_t ssfa = sb + Cfg::kBTile;
+          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+          const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
+          const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          // each CTA's scale tiles into its own tensor memory: A tile a at
+          // column 4a; B for K-step a, band i at column 8a + 4i
+#pragma unroll
+          for (int a = 0; a < Cfg::kAtomsK; ++a)
+            tc_cp_scales_pair(sfa_t + 4 * a, smem_desc(ssfa + 512 * a, 0, 128, 0));
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int a = 0; a < Cfg::kAtomsK; ++a)
+              tc_cp_scales_pair(sfb_t + 8 * a + 4 * i,
+                                smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
+#pragma unroll
+          for (int kk = 0; kk < Cfg::kMmas; ++kk) {
+            const uint64_t adesc = smem_desc(sa + 32 * kk, 16, 8 * BK, 2);
+            const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, 8 * BK, 2);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (NVF4) {
+              tc_mma_nvf4_pair(tmem_base, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
+                               sfb_t + 8 * kk, accum);
+            } else {
+              const uint32_t sid = static_cast<uint32_t>(kk);
+              tc_mma_mxf8_pair(tmem_base, adesc, bdesc, Cfg::kIdesc | (sid << 4) | (sid << 29),
+                               sfa_t, sfb_t, accum);
+            }
+          }
+          tc_commit_pair_mc(empty_bar(stage), 0x3);  // stage free in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        // accumulator ready in both CTAs (the test hook withholds the first
+        // arrival of cluster 0 so that the epilogues' bounded waits run out)
+        if (!((p.inject & 1) && blockIdx.x == 0 && t == unit0)) tc_commit_pair_mc(tfull_bar, 0x3);
+        acc_phase ^= 1u;
+      }
+      tc_commit_pair(drain_bar);
+      mbar_wait_drain(drain_bar, 0, p.status, p.timeout_ns);
+    }
+  }
+  // ------------------------------------------------------------ epilogue (both CTAs)
+  else {
+    const uint32_t ew = warp - 2;
+    const uint32_t quarter = warp & 3u;
+    const uint32_t col0 = 128u * (ew >> 2);
+    const uint32_t tempty_even = mapa_shared(tempty_bar, 0);
+    uint32_t acc_phase = 0;
+    for (int64_t t = unit0; t < total_units; t += ustride) {
+      const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, rank);
+      if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      uint32_t v[4][32];
+      const bool has_k = ti.kb_count > 0;
+      if (has_k) {
+        const uint32_t taddr = tmem_base + ((32u * quarter) << 16) + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, v[c]);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even);
+      acc_phase ^= 1u;
+      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no copy, commit or remote arrival still targets either CTA
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
   }
 }
 
@@ -554,6 +869,31 @@ bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t 
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner_bytes, rows, inner_bytes,
                       static_cast<uint32_t>(bk), box_rows,
                       bk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// Launch as 2-CTA clusters: as many co-resident clusters as the device holds
+// (one CTA per SM), at most max_units of them.
+template <typename Kern, typename... Args>
+cudaError_t launch_clusters(Kern kern, int threads, size_t smem, int64_t max_units, int num_sms,
+                            cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
+    clusters = num_sms / 2;
+  const int64_t n = max_units < clusters ? max_units : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR, int BK>
@@ -571,33 +911,34 @@ cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const G
     kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
     return cudaGetLastError();
   }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // as many co-resident 2-CTA clusters as the device holds (one CTA per SM)
-  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1), 1, 1);
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1)
-    clusters = num_sms / 2;
-  const int64_t n = max_units < clusters ? max_units : clusters;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * n), 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  return launch_clusters(kern, Cfg::kThreads, smem, max_units, num_sms, stream, ta, tb, p);
+}
+
+template <int STAGES, bool NVF4>
+cudaError_t launch_pair_variant(const CUtensorMap& ta, const CUtensorMap& tb,
+                                const CUtensorMap& tsa, const CUtensorMap& tsb,
+                                const GemmParams& p, int64_t max_units, int num_sms,
+                                cudaStream_t stream) {
+  using Cfg = PairCfg<STAGES, NVF4>;
+  auto kern = grouped_gemm_pair_kernel<STAGES, NVF4>;
+  const size_t smem = Cfg::smem_bytes(p.G);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (max_units <= 0) return cudaSuccess;
+  return launch_clusters(kern, Cfg::kThreads, smem, max_units, num_sms, stream, ta, tb, tsa, tsb,
+                         p);
 }
 
 }  // namespace
 
-// Tile width: 256 when the output tile dimension allows it (one accumulator
-// stage, 8 epilogue warps), else 128 (two accumulator stages).  pair = 1
-// launches 2-CTA clusters sharing each B tile by multicast.  The environment
-// variables MXG_GEMM_TILE_N=128 and MXG_GEMM_PAIR=0/1 override the choice.
+// Kernel choice.  Default (tile_n = 0): the CTA-pair kernel, 256 x 256
+// units, whenever the output width is a multiple of 256 and a stage holds
+// 128 bytes of K (everything but NVFP4 wgrad and NVFP4 fprop with K % 256);
+// otherwise the single-CTA kernel.  tile_n = 256 or 128 forces the
+// single-CTA kernel with that tile width (256 needs a width that allows it).
+// pair = 1 selects the single-CTA kernel's multicast variant (two CTAs of a
+// cluster share one B tile).
 cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const uint8_t* a_sf,
                                 const float* a_outer, const void* b_data, const uint8_t* b_sf,
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
@@ -644,6 +985,29 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.kb_uniform = mode == 0 ? (nvfp4 ? K / 2 : K) / BKB : (mode == 2 ? N / BKB : 0);
   p.out_cols = mode == 0 ? N : K;
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
+
+  // default: the CTA-pair kernel (256 x 256 units) wherever the output width
+  // allows it and the stage is 128 bytes of K
+  if (tile_n == 0 && !pair && BKB == 128 && bn == 256) {
+    CUtensorMap ta, tb, tsa, tsb;
+    const int atoms = nvfp4 ? 4 : 1;  // scale tiles along K per stage and band
+    const uint64_t b_bands = static_cast<uint64_t>(b_rows / 128);
+    const uint64_t sfb_dims[3] = {128, static_cast<uint64_t>(p.b_atoms_row), b_bands};
+    const uint64_t sfb_strides[2] = {512, static_cast<uint64_t>(512 * p.b_atoms_row)};
+    const uint32_t sfb_box[3] = {128, static_cast<uint32_t>(atoms), 2};
+    const int64_t ebn = nvfp4 ? 1 : 2;  // bytes per element x 2
+    if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows, 128, 128) ||
+        !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows, 128, 128) ||
+        !make_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128,
+                      static_cast<uint64_t>((a_rows / 128) * p.a_atoms_row), 512, 128,
+                      static_cast<uint32_t>(atoms), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, sfb_dims, sfb_strides, sfb_box))
+      return cudaErrorInvalidValue;
+    const int64_t units = mode == 1 ? G * (((N / 128) + 1) / 2) * (K / 256)
+                                    : (((M_cap / 128) + G + 1) / 2) * (p.out_cols / 256);
+    if (nvfp4) return launch_pair_variant<5, true>(ta, tb, tsa, tsb, p, units, num_sms, stream);
+    return launch_pair_variant<6, false>(ta, tb, tsa, tsb, p, units, num_sms, stream);
+  }
 
   const bool pr = pair != 0;
   const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2

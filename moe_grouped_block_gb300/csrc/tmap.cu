@@ -36,4 +36,17 @@ bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                  const uint64_t strides_bytes[2], const uint32_t box[3]) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t b[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dtype, 3, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mxg

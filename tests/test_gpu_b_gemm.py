@@ -65,7 +65,26 @@ def test_single_tile_one_hot():
     assert torch.equal(C.cpu(), w[0].t().contiguous())
 
 
-@pytest.mark.parametrize("tn", [None, 128])
+def test_pair_unit_upper_half_past_end():
+    # one expert of 128 rows, N = 256: the CTA-pair kernel's odd CTA reads rows
+    # 128..255, past the end of A (zero fill), and must store nothing
+    G, N, K, M = 1, 256, 256, 128
+    xf = torch.zeros((M, K))
+    xf[torch.arange(M), torch.arange(M) + 64] = 1.0
+    w = torch.randint(-8, 9, (G, N, K)).float()
+    sizes = torch.tensor([M], dtype=torch.int32)
+    ws, st = gpu_offsets(sizes, K, M)
+    qx, _ = gpu_mxfp8(xf.to(torch.bfloat16).to(DEV), ws, G, mxg.MXG_ROWWISE)
+    qw, _ = gpu_mxfp8(w.to(torch.bfloat16).to(DEV).reshape(N, K), None, 1, mxg.MXG_ROWWISE)
+    C = torch.full((M, N), 7.0, device=DEV)
+    mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, (qx["q_row"], qx["sf_row"], None),
+                         (qw["q_row"], qw["sf_row"], None), ws, G, M, N, K, C=C, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(C.cpu(), w[0][:, 64:64 + M].t().contiguous())
+
+
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_fprop_tiny_workload(tn):
     wl = workloads.WORKLOADS["tiny_fprop_mxfp8"]
     case, offs, rows, ref = _run_fprop(wl, tn)
@@ -74,7 +93,7 @@ def test_fprop_tiny_workload(tn):
     assert errs.max() <= TOL, errs
 
 
-@pytest.mark.parametrize("tn", [None, 128])
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_fprop_mixtral_shape_scaled(tn):
     wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=2048, K=512, N=512)
     case, offs, rows, ref = _run_fprop(wl, tn)
@@ -105,7 +124,7 @@ def test_fprop_alpha_beta_and_capacity_padding():
     assert np.array_equal(got[wl.M:], c_in.numpy()[wl.M:].astype(np.float64))
 
 
-@pytest.mark.parametrize("tn", [None, 128])
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_fprop_per_group_bias(tn):
     wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=256, N=512)
     bias = np.random.default_rng(3).standard_normal((wl.G, wl.N)).astype(np.float32)
@@ -114,7 +133,7 @@ def test_fprop_per_group_bias(tn):
     assert errs.max() <= TOL, errs
 
 
-@pytest.mark.parametrize("tn", [None, 128])
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_fprop_bf16_output(tn):
     wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=256, N=512)
     case, offs, rows, ref = _run_fprop(wl, tn, out_type=mxg.MXG_OUT_BF16)
@@ -154,9 +173,10 @@ def _wgrad_case(wl, tn=None, beta=None):
     return dW.cpu().numpy().astype(np.float64), ref, offs
 
 
-@pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (128, 512)])
-def test_wgrad_scaled(tn, K):
-    wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=2048, K=K, N=256)
+@pytest.mark.parametrize("tn,K,N", [(None, 512, 256), (None, 512, 384), (None, 384, 256),
+                                    (256, 512, 256), (128, 512, 256)])
+def test_wgrad_scaled(tn, K, N):
+    wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=2048, K=K, N=N)
     sizes = workloads.group_sizes(wl)
     got, ref, offs = _wgrad_case(wl, tn)
     for g in range(wl.G):
@@ -178,7 +198,7 @@ def test_wgrad_empty_group_beta():
 
 
 # --------------------------------------------------------------------------- NVFP4
-@pytest.mark.parametrize("tn", [None, 128])
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_nvfp4_fprop_scaled(tn):
     wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=4096, K=512, N=512)
     case, offs, rows, ref = _run_fprop(wl, tn)
@@ -195,7 +215,7 @@ def test_nvfp4_fprop_alpha():
 
 
 # --------------------------------------------------------------------------- dgrad
-@pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (128, 256)])
+@pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (256, 512), (128, 256)])
 def test_dgrad_scaled(tn, K):
     """dX = dY . W_g: rowwise dY, colwise (transposed) copy of W."""
     wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=2048, K=K, N=256, G=8)

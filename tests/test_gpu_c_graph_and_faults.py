@@ -120,7 +120,7 @@ def test_bad_group_sizes_are_flagged_and_clamped(routing, bits):
     assert np.all(qx["q_row"][live:].cpu().numpy() == 0x77)
 
 
-@pytest.mark.parametrize("tn", [None, 128])
+@pytest.mark.parametrize("tn", [None, 256, 128])
 def test_bounded_wait_runs_out_and_the_device_stays_usable(tn):
     """A flag that nothing sets: CTA 0 withholds its first accumulator-ready
     arrival, so its epilogue's wait runs out after 20 ms.  The launch must
