@@ -58,6 +58,7 @@ struct GemmParams {
   int out_bf16;
   int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
   int prefetch;  // L2 prefetch distance in K blocks (0 = off)
+  int c_align32;  // C is 32-byte aligned (whole-sector epilogue stores)
 };
 
 // BK: bytes of K per pipeline stage (128 with the 128-byte swizzle, or 64
@@ -243,17 +244,25 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
   if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
 }
 
+// 32 bytes to global memory in one store (the address is 32-byte aligned).
+__device__ __forceinline__ void st_global_32B(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // One output row of the epilogue: 128 accumulator columns (v, four loads of
 // 32) starting at column c_col + col0, with alpha, the NVFP4 outer scales,
 // bias and beta applied, stored as fp32 or bf16.  Rows at or beyond the
-// tile's row_end are skipped.
+// tile's row_end are skipped.  Each thread owns a row, so a store instruction
+// touches 32 rows: with a 32-byte-aligned C every store fills whole 32-byte
+// sectors (16 bf16 or 8 fp32 per store), else 16-byte stores are used.
 template <bool NVF4>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
                                              uint32_t col0, const uint32_t (&v)[4][32],
                                              bool has_k) {
   if (row >= ti.row_end) return;
-  const int64_t ldc = p.out_cols;
-  const int64_t cbase = row * ldc + ti.c_col + col0;
+  const int64_t cbase = row * p.out_cols + ti.c_col + col0;
   const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
   const float beta = p.beta ? p.beta[ti.g] : 0.0f;
   float rs = 1.0f;
@@ -264,42 +273,61 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
     rs = p.a_outer[row];
     cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
   }
+  // value of accumulator column j = 32c + e after alpha, outer scales and bias
+  auto value = [&](int c, int e) {
+    const int j = 32 * c + e;
+    float a = has_k ? __uint_as_float(v[c][e]) : 0.0f;
+    if (NVF4) a = a * rs * cs[j];
+    float o = alpha * a;
+    if (bs) o += bs[j];
+    return o;
+  };
+  if (p.out_bf16) {
+    uint16_t* out = static_cast<uint16_t*>(p.C) + cbase;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 4; ++c) {
 #pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) {
-      float o[4];
+      for (int h = 0; h < 2; ++h) {  // 16 columns = 32 bytes
+        uint16_t* dst = out + 32 * c + 16 * h;
+        uint32_t w[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float a = has_k ? __uint_as_float(v[c][4 * q4 + e]) : 0.0f;
-        if (NVF4) a = a * rs * cs[32 * c + 4 * q4 + e];
-        o[e] = alpha * a;
-        if (bs) o[e] += bs[32 * c + 4 * q4 + e];
-      }
-      const int64_t idx = cbase + 32 * c + 4 * q4;
-      if (beta != 0.0f) {
-        if (p.out_bf16) {
-          const uint2 old = *reinterpret_cast<const uint2*>(static_cast<uint16_t*>(p.C) + idx);
-          o[0] += beta * bf16lo(old.x);
-          o[1] += beta * bf16hi(old.x);
-          o[2] += beta * bf16lo(old.y);
-          o[3] += beta * bf16hi(old.y);
+        for (int q = 0; q < 8; ++q) {
+          float o0 = value(c, 16 * h + 2 * q), o1 = value(c, 16 * h + 2 * q + 1);
+          if (beta != 0.0f) {
+            const uint32_t old = reinterpret_cast<const uint32_t*>(dst)[q];
+            o0 += beta * bf16lo(old);
+            o1 += beta * bf16hi(old);
+          }
+          w[q] = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
+        }
+        if (p.c_align32) {
+          st_global_32B(dst, w);
         } else {
-          const float4 old = *reinterpret_cast<const float4*>(static_cast<float*>(p.C) + idx);
-          o[0] += beta * old.x;
-          o[1] += beta * old.y;
-          o[2] += beta * old.z;
-          o[3] += beta * old.w;
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
-      if (p.out_bf16) {
-        uint2 w;
-        w.x = f32_to_bf16_bits(o[0]) | (f32_to_bf16_bits(o[1]) << 16);
-        w.y = f32_to_bf16_bits(o[2]) | (f32_to_bf16_bits(o[3]) << 16);
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.C) + idx) = w;
-      } else {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.C) + idx) =
-            make_float4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    float* out = static_cast<float*>(p.C) + cbase;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {  // 8 columns = 32 bytes
+        float* dst = out + 32 * c + 8 * h;
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float o = value(c, 8 * h + q);
+          if (beta != 0.0f) o += beta * dst[q];
+          w[q] = __float_as_uint(o);
+        }
+        if (p.c_align32) {
+          st_global_32B(dst, w);
+        } else {
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
     }
   }
@@ -574,7 +602,11 @@ template <int STAGES, bool NVF4>
 struct PairCfg {
   static constexpr int BN = 256, BK = 128;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  // scale-copy warps (even CTA): each tcgen05 instruction costs the issuing
+  // thread about as long as a quarter of a stage's MMA work, so the scale
+  // copies run on their own warps, beside the MMA thread
+  static constexpr int kSfWarps = NVF4 ? 2 : 1;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kSfWarps);
   static constexpr int kATile = 128 * BK;  // this CTA's rows of A
   static constexpr int kBTile = 128 * BK;  // this CTA's half of B
   static constexpr int kMmas = BK / 32;
@@ -589,8 +621,9 @@ struct PairCfg {
   static constexpr int kSfCols = kSfaCols * 3;
   static constexpr int kTmemCols = 512;
   static_assert(BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
-  // full[S], empty[S], tfull, tempty, drain; TMEM base; abort flag
-  static constexpr int kBarBytes = 8 * (2 * STAGES + 3) + 16;
+  static constexpr int kSfCopies = 3 * kAtomsK;  // scale tiles per stage (A, then B bands)
+  // full[S], empty[S], sfready[S], tfull, tempty, drain, sfdrain; TMEM base; abort flag
+  static constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
   static size_t smem_bytes(int G) {
     return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 8 * (G + 1) + 16;
   }
@@ -664,7 +697,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * STAGES + 3));
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
@@ -674,19 +707,24 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-  const uint32_t tfull_bar = smem_u32(&bars[2 * STAGES]);
-  const uint32_t tempty_bar = smem_u32(&bars[2 * STAGES + 1]);
-  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 2]);
+  auto sfready_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + s]); };
+  const uint32_t tfull_bar = smem_u32(&bars[3 * STAGES]);
+  const uint32_t tempty_bar = smem_u32(&bars[3 * STAGES + 1]);
+  const uint32_t drain_bar = smem_u32(&bars[3 * STAGES + 2]);
+  const uint32_t sfdrain_bar = smem_u32(&bars[3 * STAGES + 3]);
+  constexpr uint32_t kFirstSfWarp = 2 + Cfg::kEpiWarps;
 
   // ------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);   // even CTA: its producer's arrival + both CTAs' bytes
       mbar_init(empty_bar(s), 1);  // the pair's MMA commit
+      mbar_init(sfready_bar(s), Cfg::kSfWarps);  // even CTA: the scale-copy warps' commits
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 2 * Cfg::kEpiWarps);  // even CTA: both CTAs' epilogue warps
     mbar_init(drain_bar, 1);
+    mbar_init(sfdrain_bar, Cfg::kSfWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -768,32 +806,24 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
         if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+          // operands landed, and their scale tiles are in tensor memory
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns) ||
+              !mbar_wait(sfready_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t sa = smem_base + stage * Cfg::kStageBytes;
           const uint32_t sb = sa + Cfg::kATile;
-          const uint32_t ssfa = sb + Cfg::kBTile;
-          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
           const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-          // each CTA's scale tiles into its own tensor memory: A tile a at
-          // column 4a; B for K-step a, band i at column 8a + 4i
-#pragma unroll
-          for (int a = 0; a < Cfg::kAtomsK; ++a)
-            tc_cp_scales_pair(sfa_t + 4 * a, smem_desc(ssfa + 512 * a, 0, 128, 0));
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-#pragma unroll
-            for (int a = 0; a < Cfg::kAtomsK; ++a)
-              tc_cp_scales_pair(sfb_t + 8 * a + 4 * i,
-                                smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
+          const uint64_t adesc0 = smem_desc(sa, 16, 8 * BK, 2);
+          const uint64_t bdesc0 = smem_desc(sb, 16, 8 * BK, 2);
 #pragma unroll
           for (int kk = 0; kk < Cfg::kMmas; ++kk) {
-            const uint64_t adesc = smem_desc(sa + 32 * kk, 16, 8 * BK, 2);
-            const uint64_t bdesc = smem_desc(sb + 32 * kk, 16, 8 * BK, 2);
+            // K step kk starts 32 bytes further along the row (16-byte units)
+            const uint64_t adesc = adesc0 + 2 * kk;
+            const uint64_t bdesc = bdesc0 + 2 * kk;
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (NVF4) {
               tc_mma_nvf4_pair(tmem_base, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
@@ -818,6 +848,51 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       }
       tc_commit_pair(drain_bar);
       mbar_wait_drain(drain_bar, 0, p.status, p.timeout_ns);
+    }
+  }
+  // ------------------------------------------------------------ scale copies (even CTA)
+  else if (warp >= kFirstSfWarp) {
+    if (lane == 0 && rank == 0) {
+      const int j = static_cast<int>(warp - kFirstSfWarp);
+      uint32_t stage = 0, phase = 0;
+      for (int64_t t = unit0; t < total_units; t += ustride) {
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, 0);
+        bool ok = true;
+        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+          // the stage's previous MMAs finished before its producer refilled it
+          // (empty barrier), so its scale columns are free once it is full
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ssfa = smem_base + stage * Cfg::kStageBytes + Cfg::kATile + Cfg::kBTile;
+          const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
+          const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
+          const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          // copy c: A tile a = c at column 4a; B (band i, K-step a) at 8a + 4i
+#pragma unroll
+          for (int c = 0; c < Cfg::kSfCopies; ++c) {
+            if (c % Cfg::kSfWarps != j) continue;
+            if (c < Cfg::kAtomsK) {
+              tc_cp_scales_pair(sfa_t + 4 * c, smem_desc(ssfa + 512 * c, 0, 128, 0));
+            } else {
+              const int i = (c - Cfg::kAtomsK) / Cfg::kAtomsK, a = (c - Cfg::kAtomsK) % Cfg::kAtomsK;
+              tc_cp_scales_pair(sfb_t + 8 * a + 4 * i,
+                                smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
+            }
+          }
+          tc_commit_pair(sfready_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // every copy this thread issued has completed before TMEM is freed
+      tc_commit_pair(sfdrain_bar);
+      mbar_wait_drain(sfdrain_bar, 0, p.status, p.timeout_ns);
     }
   }
   // ------------------------------------------------------------ epilogue (both CTAs)
@@ -959,6 +1034,7 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.beta = beta;
   p.bias = bias;
   p.C = C;
+  p.c_align32 = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 ? 1 : 0;
   p.status = status;
   p.M_cap = M_cap;
   p.N = N;
