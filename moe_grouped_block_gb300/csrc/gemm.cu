@@ -195,7 +195,7 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
                                                    bool pair_units, int bn) {
   int64_t carry_rows = 0, carry_tiles = 0;
   int32_t bits = 0;
-  const int64_t ntiles_n = p.out_cols / bn;
+  const int64_t ntiles_n = (p.out_cols + bn - 1) / bn;  // a last unit may be half wide
   for (int base = 0; base < p.G; base += 32) {
     const int g = base + static_cast<int>(lane);
     int64_t s = 0;
@@ -254,14 +254,15 @@ __device__ __forceinline__ void st_global_32B(void* ptr, const uint32_t (&w)[8])
 // One output row of the epilogue: 128 accumulator columns (v, four loads of
 // 32) starting at column c_col + col0, with alpha, the NVFP4 outer scales,
 // bias and beta applied, stored as fp32 or bf16.  Rows at or beyond the
-// tile's row_end are skipped.  Each thread owns a row, so a store instruction
+// tile's row_end, and the upper half of a half-wide last column unit, are
+// skipped.  Each thread owns a row, so a store instruction
 // touches 32 rows: with a 32-byte-aligned C every store fills whole 32-byte
 // sectors (16 bf16 or 8 fp32 per store), else 16-byte stores are used.
 template <bool NVF4>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
                                              uint32_t col0, const uint32_t (&v)[4][32],
                                              bool has_k) {
-  if (row >= ti.row_end) return;
+  if (row >= ti.row_end || ti.c_col + col0 >= p.out_cols) return;
   const int64_t cbase = row * p.out_cols + ti.c_col + col0;
   const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
   const float beta = p.beta ? p.beta[ti.g] : 0.0f;
@@ -636,6 +637,9 @@ struct PairCfg {
 // Work unit t -> this CTA's half.  fprop / dgrad: 256 rows of one group (the
 // upper half may run past the group's end: it is computed but not stored)
 // times 256 output columns.  wgrad: 256 rows of dW_g times 256 columns.
+// When the output width is an odd multiple of 128 the last column unit is
+// half wide: its upper 128 B rows are loaded (another group's rows, or the
+// zero fill past the tensor's end) but those columns are not stored.
 // a_row is this CTA's first A row; b_row is the unit's first B row (this CTA
 // loads b_row + 128 * rank).
 template <int EPB>
@@ -668,7 +672,7 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     ti.c_col = 256 * n_tile;
     ti.row_end = row_off[g + 1];
   } else {
-    const int64_t nu = ((p.N >> 7) + 1) >> 1, kt = p.K / 256, tpg = nu * kt;
+    const int64_t nu = ((p.N >> 7) + 1) >> 1, kt = (p.K + 255) / 256, tpg = nu * kt;
     const int g = static_cast<int>(t / tpg);
     const int64_t local = t % tpg;
     const int64_t nu_i = local / kt, k_tile = local % kt;
@@ -742,7 +746,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
   const int64_t ustride = gridDim.x >> 1;
   const int64_t total_units =
       p.mode != 1 ? static_cast<int64_t>(tile_off[p.G])
-                  : p.G * ((((p.N >> 7) + 1) >> 1) * (p.K / 256));
+                  : p.G * ((((p.N >> 7) + 1) >> 1) * ((p.K + 255) / 256));
 
   // ------------------------------------------------------------ producers (both CTAs)
   if (warp == 0) {
@@ -1008,9 +1012,9 @@ cudaError_t launch_pair_variant(const CUtensorMap& ta, const CUtensorMap& tb,
 }  // namespace
 
 // Kernel choice.  Default (tile_n = 0): the CTA-pair kernel, 256 x 256
-// units, whenever the output width is a multiple of 256 and a stage holds
-// 128 bytes of K (everything but NVFP4 wgrad and NVFP4 fprop with K % 256);
-// otherwise the single-CTA kernel.  tile_n = 256 or 128 forces the
+// units, whenever a stage holds 128 bytes of K (everything but NVFP4 wgrad and
+// NVFP4 fprop with K % 256) and B has at least 256 rows; otherwise the
+// single-CTA kernel.  tile_n = 256 or 128 forces the
 // single-CTA kernel with that tile width (256 needs a width that allows it).
 // pair = 1 selects the single-CTA kernel's multicast variant (two CTAs of a
 // cluster share one B tile).
@@ -1062,9 +1066,9 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.out_cols = mode == 0 ? N : K;
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
-  // default: the CTA-pair kernel (256 x 256 units) wherever the output width
-  // allows it and the stage is 128 bytes of K
-  if (tile_n == 0 && !pair && BKB == 128 && bn == 256) {
+  // default: the CTA-pair kernel (256 x 256 units) whenever a stage is 128
+  // bytes of K and B spans at least the two 128-row bands of one unit
+  if (tile_n == 0 && !pair && BKB == 128 && b_rows >= 256) {
     CUtensorMap ta, tb, tsa, tsb;
     const int atoms = nvfp4 ? 4 : 1;  // scale tiles along K per stage and band
     const uint64_t b_bands = static_cast<uint64_t>(b_rows / 128);
@@ -1079,8 +1083,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                       static_cast<uint32_t>(atoms), CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, sfb_dims, sfb_strides, sfb_box))
       return cudaErrorInvalidValue;
-    const int64_t units = mode == 1 ? G * (((N / 128) + 1) / 2) * (K / 256)
-                                    : (((M_cap / 128) + G + 1) / 2) * (p.out_cols / 256);
+    const int64_t units = mode == 1 ? G * (((N / 128) + 1) / 2) * ((K + 255) / 256)
+                                    : (((M_cap / 128) + G + 1) / 2) * ((p.out_cols + 255) / 256);
     if (nvfp4) return launch_pair_variant<5, true>(ta, tb, tsa, tsb, p, units, num_sms, stream);
     return launch_pair_variant<6, false>(ta, tb, tsa, tsb, p, units, num_sms, stream);
   }

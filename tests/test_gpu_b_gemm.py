@@ -143,6 +143,30 @@ def test_fprop_bf16_output(tn):
     assert np.all(np.abs(got - refb) <= ulp + 1e-6 * np.abs(ref).max())
 
 
+@pytest.mark.parametrize("out_type", [mxg.MXG_OUT_F32, mxg.MXG_OUT_BF16])
+def test_fprop_half_wide_last_column_unit(out_type):
+    # N = 384: the CTA-pair kernel's last 256-wide column unit is half wide; its
+    # upper 128 columns (the next expert's weight rows, or the zero fill past
+    # the end) are computed but never stored
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=256, N=384)
+    bias = np.random.default_rng(5).standard_normal((wl.G, wl.N)).astype(np.float32)
+    case, offs, rows, ref = _run_fprop(wl, bias=bias, out_type=out_type)
+    got = case["C"].cpu().float().numpy().astype(np.float64)[:wl.M]
+    if out_type == mxg.MXG_OUT_BF16:
+        refb = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        assert np.all(np.abs(got - refb) <= np.abs(refb) * 2.0 ** -7 + 1e-6 * np.abs(ref).max())
+    else:
+        errs = normwise_errors(got, ref, offs)
+        assert errs.max() <= TOL, errs
+
+
+def test_nvfp4_fprop_half_wide_last_column_unit():
+    wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=1024, K=256, N=384, G=4)
+    case, offs, rows, ref = _run_fprop(wl)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
 # --------------------------------------------------------------------------- wgrad
 def _wgrad_case(wl, tn=None, beta=None):
     inp = workloads.make_inputs(wl)
