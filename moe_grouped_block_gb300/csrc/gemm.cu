@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) mbar_arrive_relaxed(tempty_bar(acc));  // no memory published
       if (++acc == ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -606,7 +606,7 @@ struct PairCfg {
   // scale-copy warps (even CTA): each tcgen05 instruction costs the issuing
   // thread about as long as a quarter of a stage's MMA work, so the scale
   // copies run on their own warps, beside the MMA thread
-  static constexpr int kSfWarps = NVF4 ? 2 : 1;
+  static constexpr int kSfWarps = 2;
   static constexpr int kThreads = 32 * (2 + kEpiWarps + kSfWarps);
   static constexpr int kATile = 128 * BK;  // this CTA's rows of A
   static constexpr int kBTile = 128 * BK;  // this CTA's half of B
@@ -918,9 +918,12 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, v[c]);
         tmem_ld_wait();
       }
+      // the loads have completed (wait::ld): TMEM may be overwritten.  The
+      // arrival is relaxed so that it does not wait for this warp's stores
+      // of the previous unit to drain
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_even);
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_even);
       acc_phase ^= 1u;
       epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k);
     }
