@@ -244,13 +244,6 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
   if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
 }
 
-// 32 bytes to global memory in one store (the address is 32-byte aligned).
-__device__ __forceinline__ void st_global_32B(void* ptr, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
-               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
-
 // One output row of the epilogue: 128 accumulator columns (v, four loads of
 // 32) starting at column c_col + col0, with alpha, the NVFP4 outer scales,
 // bias and beta applied, stored as fp32 or bf16.  Rows at or beyond the

@@ -418,6 +418,35 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
   return u >> 16;
 }
 
+// ---------------------------------------------------------------- packed bf16
+// max(|a|, |b|) per 16-bit half; the sign bit of the result is the XOR of the
+// inputs' signs and carries no meaning here.  Exact.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Per-half product, round to nearest even.  Exact when one factor is a power
+// of two and the product is a normal bf16.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16 bits of 2^-e for e in [-127, 126] (a normal power of two).
+__device__ __forceinline__ uint32_t bf16_pow2_neg_bits(int e) {
+  return static_cast<uint32_t>(127 - e) << 7;
+}
+
+// 32 bytes to global memory in one store (the address is 32-byte aligned).
+__device__ __forceinline__ void st_global_32B(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------------- MX scale rule
 // e = ceil(log2(amax / 448)) clamped to [-127, 127]; amax = 0 (or an fp32
 // subnormal) gives -127.  With amax = 1.f * 2^E: e = E - 8 + (1.f > 1.75).

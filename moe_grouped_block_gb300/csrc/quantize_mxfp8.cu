@@ -26,6 +26,12 @@
 //            conflicts) -- once for the 32x1 block amax of both columns, once
 //            to quantize -- and writes 32 contiguous bytes of each transposed
 //            row.
+//   arithmetic: amax and the scaling by 2^-e run on packed bf16 pairs.  The
+//            maximum of magnitudes is exact; so is the product by a power of
+//            two whenever it is a normal bf16 (|x| 2^-e <= 448 bounds it
+//            above), and a product below the normal range is under 2^-126,
+//            which the E4M3 conversion takes to a signed zero in any case.
+//            Only that final conversion goes through fp32.
 #include "mxg_device.cuh"
 #include "mxg_host.h"
 
@@ -66,22 +72,20 @@ __device__ __forceinline__ int64_t live_rows_warp(const int64_t* ws, int G, int6
   return sum;
 }
 
-// 8 bf16 scaled by 2^-e -> 8 E4M3 bytes.
-__device__ __forceinline__ uint2 quant8(const uint4 v, float s) {
+// Scaled bf16 pair (already multiplied by 2^-e, exact) -> two E4M3 bytes.
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t w) { return cvt_e4m3x2(bf16lo(w), bf16hi(w)); }
+
+// 8 bf16 (one row chunk) scaled by the packed power of two s2 -> 8 E4M3 bytes.
+__device__ __forceinline__ uint2 quant8(const uint4 v, uint32_t s2) {
   uint2 o;
-  o.x = cvt_e4m3x2(bf16lo(v.x) * s, bf16hi(v.x) * s) |
-        (cvt_e4m3x2(bf16lo(v.y) * s, bf16hi(v.y) * s) << 16);
-  o.y = cvt_e4m3x2(bf16lo(v.z) * s, bf16hi(v.z) * s) |
-        (cvt_e4m3x2(bf16lo(v.w) * s, bf16hi(v.w) * s) << 16);
+  o.x = e4m3_pair(bf16x2_mul(v.x, s2)) | (e4m3_pair(bf16x2_mul(v.y, s2)) << 16);
+  o.y = e4m3_pair(bf16x2_mul(v.z, s2)) | (e4m3_pair(bf16x2_mul(v.w, s2)) << 16);
   return o;
 }
 
-__device__ __forceinline__ float amax8(const uint4 v) {
-  float a = fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x)));
-  a = fmaxf(a, fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))));
-  a = fmaxf(a, fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))));
-  return fmaxf(a, fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w))));
-}
+// |x| of the low / high bf16 of a packed value, as fp32 (exact).
+__device__ __forceinline__ float abs_lo(uint32_t m) { return __uint_as_float((m & 0x7FFFu) << 16); }
+__device__ __forceinline__ float abs_hi(uint32_t m) { return __uint_as_float(m & 0x7FFF0000u); }
 
 }  // namespace
 
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(256, 3)
     mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                           const int64_t* __restrict__ group_ws, int G, uint8_t* __restrict__ q_row,
                           uint8_t* __restrict__ sf_row, uint8_t* __restrict__ q_col,
-                          uint8_t* __restrict__ sf_col, int32_t* status) {
+                          uint8_t* __restrict__ sf_col, int qcol_v8, int32_t* status) {
   extern __shared__ uint8_t qsmem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -158,11 +162,13 @@ __global__ void __launch_bounds__(256, 3)
       for (int i = 0; i < 8; ++i) {
         const uint32_t r = i * 16 + warp * 2 + half;
         const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + cl];
-        float a = amax8(v);
+        const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w));
+        float a = fmaxf(abs_lo(m), abs_hi(m));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         const int e = mx_exponent(a);
-        const uint2 o = quant8(v, pow2_neg(e));
+        const uint32_t sb = bf16_pow2_neg_bits(e);
+        const uint2 o = quant8(v, sb | (sb << 16));
         *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
         if ((cl & 3u) == 0)
           sfr_s[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
@@ -171,41 +177,41 @@ __global__ void __launch_bounds__(256, 3)
 
     // ---- phase 2: columns (transposed output)
     if (COL) {
-      const uint32_t cp = threadIdx.x & 63u;  // column pair 2cp, 2cp+1
+      const uint32_t cp = threadIdx.x & 63u;  // column pair 2cp, 2cp+1 (one 32-bit word)
       const uint32_t j = threadIdx.x >> 6;    // 32-row block
-      // pass A: block amax of both columns; pass B: re-read and quantize
-      // (shared memory is cheap here and no 32-word register array is held)
+      // pass A: block amax of both columns at once (packed); pass B: re-read,
+      // scale both halves by their own power of two and convert.  A warp reads
+      // 32 consecutive words per row: no bank conflicts.
       const uint32_t* col = tile + (32 * j) * 64 + cp;
-      float alo = 0.f, ahi = 0.f;
+      uint32_t m = 0;
 #pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t w = col[i * 64];
-        alo = fmaxf(alo, fabsf(bf16lo(w)));
-        ahi = fmaxf(ahi, fabsf(bf16hi(w)));
-      }
-      const int elo = mx_exponent(alo), ehi = mx_exponent(ahi);
-      const float slo = pow2_neg(elo), shi = pow2_neg(ehi);
+      for (int i = 0; i < 32; ++i) m = bf16x2_max_abs(m, col[i * 64]);
+      const int elo = mx_exponent(abs_lo(m)), ehi = mx_exponent(abs_hi(m));
+      const uint32_t s2 = bf16_pow2_neg_bits(elo) | (bf16_pow2_neg_bits(ehi) << 16);
+      uint32_t olo[8], ohi[8];  // 32 E4M3 bytes of column 2cp / 2cp+1
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int e = c ? ehi : elo;
-        const float s = c ? shi : slo;
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w0 = col[(4 * i) * 64], w1 = col[(4 * i + 1) * 64];
-          const uint32_t w2 = col[(4 * i + 2) * 64], w3 = col[(4 * i + 3) * 64];
-          const float f0 = (c ? bf16hi(w0) : bf16lo(w0)) * s;
-          const float f1 = (c ? bf16hi(w1) : bf16lo(w1)) * s;
-          const float f2 = (c ? bf16hi(w2) : bf16lo(w2)) * s;
-          const float f3 = (c ? bf16hi(w3) : bf16lo(w3)) * s;
-          o[i] = cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16);
-        }
-        const uint32_t kk = 2 * cp + c;
-        uint4* dst = reinterpret_cast<uint4*>(q_col + (k0 + kk) * cap + m0 + 32 * j);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        sfc_s[(kk & 31u) * 16 + (kk >> 5) * 4 + j] = static_cast<uint8_t>(e + 127);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t u0 = bf16x2_mul(col[(4 * i) * 64], s2);
+        const uint32_t u1 = bf16x2_mul(col[(4 * i + 1) * 64], s2);
+        const uint32_t u2 = bf16x2_mul(col[(4 * i + 2) * 64], s2);
+        const uint32_t u3 = bf16x2_mul(col[(4 * i + 3) * 64], s2);
+        olo[i] = cvt_e4m3x2(bf16lo(u0), bf16lo(u1)) | (cvt_e4m3x2(bf16lo(u2), bf16lo(u3)) << 16);
+        ohi[i] = cvt_e4m3x2(bf16hi(u0), bf16hi(u1)) | (cvt_e4m3x2(bf16hi(u2), bf16hi(u3)) << 16);
       }
+      uint8_t* dlo = q_col + (k0 + 2 * cp) * cap + m0 + 32 * j;
+      uint8_t* dhi = dlo + cap;
+      if (qcol_v8) {
+        st_global_32B(dlo, olo);
+        st_global_32B(dhi, ohi);
+      } else {
+        reinterpret_cast<uint4*>(dlo)[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        reinterpret_cast<uint4*>(dlo)[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+        reinterpret_cast<uint4*>(dhi)[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+        reinterpret_cast<uint4*>(dhi)[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+      }
+      const uint32_t klo = 2 * cp, khi = klo + 1;
+      sfc_s[(klo & 31u) * 16 + (klo >> 5) * 4 + j] = static_cast<uint8_t>(elo + 127);
+      sfc_s[(khi & 31u) * 16 + (khi >> 5) * 4 + j] = static_cast<uint8_t>(ehi + 127);
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -248,8 +254,9 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kQSmemBytes);
     if (e != cudaSuccess) return e;
+    const int qcol_v8 = (reinterpret_cast<uintptr_t>(q_col) & 31u) == 0 ? 1 : 0;
     kern<<<grid, 256, kQSmemBytes, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col,
-                                              sf_col, status);
+                                              sf_col, qcol_v8, status);
     return cudaGetLastError();
   };
   if (row && col) return launch(mxfp8_quantize_kernel<true, true>);
