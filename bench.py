@@ -51,6 +51,46 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+GEMM_SOURCES = ("gemm.cu", "mxg_device.cuh", "mxg_host.h", "tmap.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "grouped_gemm_pair_kernel_dram_traffic.md")
+
+
+def gemm_source_digest() -> str:
+    """sha256 over the GEMM kernel's sources, in a fixed order: a DRAM traffic
+    figure is reported only while the kernel it was measured on is unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "moe_grouped_block_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) of one GEMM launch of this workload, from the
+    committed ncu summary, or None if there is none or the sources changed
+    since it was taken.  The summary's table rows read
+    `| workload | kernel | read bytes | write bytes | traffic bytes | ... |` and
+    it carries a line `sources sha256: <hex>`."""
+    if not os.path.exists(TRAFFIC_SUMMARY):
+        return None
+    text = open(TRAFFIC_SUMMARY).read()
+    digest = None
+    for line in text.splitlines():
+        if line.startswith("sources sha256:"):
+            digest = line.split(":", 1)[1].strip().strip("`")
+    if digest != gemm_source_digest():
+        return None
+    for line in text.splitlines():
+        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 5 and cells[0] == workload:
+            try:
+                return int(cells[4])
+            except ValueError:
+                return None
+    return None
+
+
 def max_over_ranks(value: float, dist=None, device=None) -> float:
     """MAX of a per-rank scalar over all ranks (identity without a group)."""
     if dist is None or not dist.is_initialized():
@@ -364,7 +404,10 @@ def run_mxg(args, wl, ws_world, rank, local):
     roofline = {"bound": "tensor", "kernel": gemm_name, "achieved": round(achieved, 1),
                 "peak": round(peak_tc, 1), "unit": "TFLOP/s", "frac": round(achieved / peak_tc, 4),
                 "peak_source": "%s bf16_tflops (burst) x %d" % (peak_src, 6 if nvfp4 else 2),
-                "traffic": None}
+                "traffic": measured_traffic(wl.name),
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size "
+                                  "launch (profiles/grouped_gemm_pair_kernel_dram_traffic.md); "
+                                  "null when the kernel changed since"}
     if nvfp4:  # the NVFP4 layer is HBM-bound: report the time roofline too
         b = path.kernel_bytes(gemm_name)
         roofline["hbm_bytes"] = b
