@@ -245,6 +245,73 @@ size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, 
                                         int64_t M_cap, int64_t N);
 
 /* ------------------------------------------------------------------------- */
+/* Group sizes that are not multiples of 128 (MXFP8).  [PR2763] review       */
+/* thread on the V2 alignment rule: the 128-row requirement comes from how   */
+/* the grouped quantize and the GEMM setup compute per-group scale offsets,  */
+/* not from the GEMM; [TE-gemm] grouped_gemm: padding belongs to the group   */
+/* and is zero-filled so that it does not change the result; [TE-gemm]      */
+/* apply_padding_to_scale_inv pads scale matrices of non-128 dims.  Here     */
+/* each group's scales, and its slab of a colwise copy, are padded to a      */
+/* multiple of 128 rows with zeros; rowwise data stays dense.                */
+/* ------------------------------------------------------------------------- */
+
+/* Rows of the padded layouts: rows_capacity + 128 * G (an upper bound on
+ * the sum over groups of each group's rows rounded up to 128).  Returns 0
+ * if rows_capacity < 0 or G < 1. */
+int64_t mxg_unaligned_rows_capacity(int64_t rows_capacity, int G);
+
+/* As mxg_group_offsets, but sizes are kept as given: no rounding and no
+ * MISALIGNED bit (negative sizes and rows past rows_capacity are sanitised
+ * as there).  Same workspace layout. */
+mxg_status_t mxg_group_offsets_unaligned(const void* sizes, int sizes_is_int64, int G,
+                                         int64_t multiplier, int64_t last_dim,
+                                         int64_t rows_capacity, int64_t* ws, int32_t* dev_status,
+                                         mxg_stream_t stream);
+
+/* MXFP8 grouped quantize for groups of any size.  group_ws (required) is a
+ * workspace of mxg_group_offsets_unaligned; group g owns data rows
+ * [row_off_g, row_off_g + M_g) and padded rows [prow_off_g, prow_off_g +
+ * P_g) with P_g = M_g rounded up to 128 and prow_off the prefix sum of P.
+ * With R_pad = mxg_unaligned_rows_capacity(rows_capacity, G):
+ *   q_row  : E4M3 [rows_capacity, cols], dense (row r of group g at row_off_g + r);
+ *   sf_row : E8M0 swizzled [R_pad, cols/32]; group g's scale rows start at
+ *            prow_off_g; its padding rows get byte 0;
+ *   q_col  : E4M3 [cols, R_pad], transposed; group g's slab is columns
+ *            [prow_off_g, prow_off_g + P_g), its padding columns 0x00;
+ *   sf_col : E8M0 swizzled [cols, R_pad/32]; 32-row blocks start at each
+ *            group's first row (a block never spans two groups).
+ * Each group is quantized as if it were its own tensor, zero-padded to P_g
+ * rows, with the block rules of mxg_group_quantize.  Rows and columns past
+ * the padded groups are not written.  Unused output pointers may be NULL.
+ * Errors: INVALID_ARG (null x or group_ws, G < 1 or G > 1024, bad layout,
+ * null required output), ALIGNMENT (rows_capacity or cols not multiples of
+ * 128, pointers not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
+mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
+                                          int64_t rows_capacity, int64_t cols,
+                                          const int64_t* group_ws, int G, uint8_t* q_row,
+                                          uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                                          int32_t* dev_status, mxg_stream_t stream);
+
+/* MXFP8 grouped GEMM for groups of any size (operands from
+ * mxg_group_quantize_unaligned, weights from mxg_group_quantize).  Same
+ * formulas, arguments and epilogue as mxg_grouped_gemm, with group_ws from
+ * mxg_group_offsets_unaligned and these operand shapes (R_pad as above):
+ *   FPROP_TN : A data [M_cap, K] dense, A scale [R_pad, K/32] padded;
+ *   WGRAD_NT : A = dY colwise [N, R_pad] + [N, R_pad/32], B = X colwise
+ *              [K, R_pad] + [K, R_pad/32]; each group contracts over its
+ *              padded slab (the zero padding adds nothing);
+ *   DGRAD_NN : A data [M_cap, N] dense, A scale [R_pad, N/32] padded.
+ * Output rows are the dense data rows; rows past a group are not written.
+ * Errors: as mxg_grouped_gemm, plus INVALID_ARG when B has fewer than 256
+ * rows (G * N for fprop, K otherwise). */
+mxg_status_t mxg_grouped_gemm_unaligned(mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                                        const mxg_operand_t* B, const int64_t* group_ws, int G,
+                                        int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                                        const float* beta, const float* bias, void* C,
+                                        mxg_out_t out_type, int32_t* dev_status,
+                                        mxg_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Dequantize ([PR2763] dequantizer: inverse swizzle of the scales, then    */
 /* data * scale).  Test helper; not on the timed path.                      */
 /* ------------------------------------------------------------------------- */

@@ -59,6 +59,7 @@ struct GemmParams {
   int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
   int prefetch;  // L2 prefetch distance in K blocks (0 = off)
   int c_align32;  // C is 32-byte aligned (whole-sector epilogue stores)
+  int unaligned;  // group sizes of any value (MXFP8, CTA-pair kernel only)
 };
 
 // BK: bytes of K per pipeline stage (128 with the 128-byte swizzle, or 64
@@ -102,6 +103,7 @@ struct GemmCfg {
 struct TileInfo {
   int g;
   int64_t a_row, b_row;      // first row of the A / B tile (TMA coordinate 1)
+  int64_t a_sf_row;          // row of A's scales: the padded row when groups are unaligned
   int64_t kb_count;          // K blocks (128 bytes) of this tile
   int64_t a_kb0, b_kb0;      // first K block of A and of B
   int64_t c_row, c_col;      // top-left output element
@@ -170,6 +172,7 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
   }
+  ti.a_sf_row = ti.a_row;
   return ti;
 }
 
@@ -186,16 +189,27 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 }
 
 // Group tables in shared memory, built by one warp: sanitised row offsets
-// (sizes clamped at 0, rounded down to 128, the running sum capped at
-// M_cap) and, for fprop / dgrad, each group's first work unit -- a unit is
-// one 128-row tile, or two (pair_units) -- times the column tiles of width bn.
-// CTA 0 records the sanitisation bits in the status word.
+// (sizes clamped at 0, rounded down to 128 unless p.unaligned, the running
+// sum capped at M_cap); padded row offsets (each kept size rounded up to
+// 128: where a group's scales, and its slab of a colwise copy, start when
+// groups are unaligned; equal to the row offsets otherwise), written when
+// prow_off is not null; and, for fprop / dgrad, each group's first work unit
+// -- a unit is one 128-row tile, or two (pair_units) -- times the column
+// tiles of width bn.  CTA 0 records the sanitisation bits in the status word.
 __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t* row_off,
-                                                   int32_t* tile_off, uint32_t lane,
-                                                   bool pair_units, int bn) {
-  int64_t carry_rows = 0, carry_tiles = 0;
+                                                   int32_t* prow_off, int32_t* tile_off,
+                                                   uint32_t lane, bool pair_units, int bn) {
+  int64_t carry_rows = 0, carry_pad = 0, carry_tiles = 0;
   int32_t bits = 0;
   const int64_t ntiles_n = (p.out_cols + bn - 1) / bn;  // a last unit may be half wide
+  auto scan = [&](int64_t v) {  // inclusive warp scan
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t u = __shfl_up_sync(0xFFFFFFFFu, v, d);
+      if (lane >= static_cast<uint32_t>(d)) v += u;
+    }
+    return v;
+  };
   for (int base = 0; base < p.G; base += 32) {
     const int g = base + static_cast<int>(lane);
     int64_t s = 0;
@@ -205,38 +219,33 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
         s = 0;
         bits |= MXG_DEV_NEG_SIZE;
       }
-      if (s & 127) {
+      if (!p.unaligned && (s & 127)) {
         s &= ~static_cast<int64_t>(127);
         bits |= MXG_DEV_MISALIGNED;
       }
       if (s > p.M_cap) s = p.M_cap;
     }
-    int64_t incl = s;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-      if (lane >= static_cast<uint32_t>(d)) incl += v;
-    }
+    const int64_t incl = scan(s);
     const int64_t before = min(carry_rows + incl - s, p.M_cap);
     const int64_t after = min(carry_rows + incl, p.M_cap);
     if (carry_rows + incl > p.M_cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
-    const int64_t mt_g = (after - before) >> 7;
+    const int64_t pad = ((after - before) + 127) & ~static_cast<int64_t>(127);
+    const int64_t pincl = scan(pad);
+    const int64_t mt_g = pad >> 7;
     const int64_t tiles_g = p.mode != 1 ? (pair_units ? (mt_g + 1) >> 1 : mt_g) * ntiles_n : 0;
-    int64_t tincl = tiles_g;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int64_t v = __shfl_up_sync(0xFFFFFFFFu, tincl, d);
-      if (lane >= static_cast<uint32_t>(d)) tincl += v;
-    }
+    const int64_t tincl = scan(tiles_g);
     if (g < p.G) {
       row_off[g] = static_cast<int32_t>(before);
+      if (prow_off) prow_off[g] = static_cast<int32_t>(carry_pad + pincl - pad);
       tile_off[g] = static_cast<int32_t>(carry_tiles + tincl - tiles_g);
     }
     carry_rows += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    carry_pad += __shfl_sync(0xFFFFFFFFu, pincl, 31);
     carry_tiles += __shfl_sync(0xFFFFFFFFu, tincl, 31);
   }
   if (lane == 0) {
     row_off[p.G] = static_cast<int32_t>(min(carry_rows, p.M_cap));
+    if (prow_off) prow_off[p.G] = static_cast<int32_t>(carry_pad);
     tile_off[p.G] = static_cast<int32_t>(carry_tiles);
   }
 #pragma unroll
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     tmem_alloc(smem_u32(tmem_base_s), Cfg::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 1) build_group_tables(p, row_off, tile_off, lane, PAIR, BN);
+  if (warp == 1) build_group_tables(p, row_off, nullptr, tile_off, lane, PAIR, BN);
   tc_fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();  // the partner's barriers exist before any multicast
@@ -501,7 +510,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
             for (int a = 0; a < Cfg::kAtomsK; ++a)
               tc_cp_scales(sfb_t + a * 4 * (BN / 128) + 4 * i,
                            smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
-#pragma unroll
           // MXFP8: byte (K block within the 128-element scale tile) of each MMA
           const uint32_t sf_id0 = NVF4 ? 0u : static_cast<uint32_t>(((ti.a_kb0 + kb) * BK & 127) >> 5);
 #pragma unroll
@@ -619,7 +627,7 @@ struct PairCfg {
   // full[S], empty[S], sfready[S], tfull, tempty, drain, sfdrain; TMEM base; abort flag
   static constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
   static size_t smem_bytes(int G) {
-    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 8 * (G + 1) + 16;
+    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16;
   }
   // M = 256 (the pair), N = 256; other fields as in GemmCfg
   static constexpr uint32_t kIdesc = (NVF4 ? ((1u << 7) | (1u << 10)) : 0u) |
@@ -634,11 +642,14 @@ struct PairCfg {
 // half wide: its upper 128 B rows are loaded (another group's rows, or the
 // zero fill past the tensor's end) but those columns are not stored.
 // a_row is this CTA's first A row; b_row is the unit's first B row (this CTA
-// loads b_row + 128 * rank).
+// loads b_row + 128 * rank).  Row units and the wgrad contraction are counted
+// on the padded offsets, so unaligned groups (a last 128-row tile partly past
+// the group) need nothing else: A's data rows start at the group's row
+// offset, its scale rows (a_sf_row) and its colwise slabs at the padded one.
 template <int EPB>
 __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p,
-                                                  const int32_t* row_off, const int32_t* tile_off,
-                                                  uint32_t rank) {
+                                                  const int32_t* row_off, const int32_t* prow_off,
+                                                  const int32_t* tile_off, uint32_t rank) {
   constexpr int BK = 128;
   TileInfo ti;
   ti.dup = false;
@@ -652,11 +663,12 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
         hi = mid;
     }
     const int g = lo;
-    const int64_t mu = (((row_off[g + 1] - row_off[g]) >> 7) + 1) >> 1;
+    const int64_t mu = (((prow_off[g + 1] - prow_off[g]) >> 7) + 1) >> 1;
     const int64_t local = t - tile_off[g];
     const int64_t n_tile = local / mu, mu_i = local % mu;
     ti.g = g;
     ti.a_row = row_off[g] + 256 * mu_i + 128 * rank;
+    ti.a_sf_row = prow_off[g] + 256 * mu_i + 128 * rank;
     ti.b_row = (p.mode == 0 ? static_cast<int64_t>(g) * p.N : 0) + 256 * n_tile;
     ti.kb_count = p.kb_uniform;
     ti.a_kb0 = 0;
@@ -671,9 +683,10 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     const int64_t nu_i = local / kt, k_tile = local % kt;
     ti.g = g;
     ti.a_row = 256 * nu_i + 128 * rank;
+    ti.a_sf_row = ti.a_row;
     ti.b_row = 256 * k_tile;
-    ti.kb_count = (row_off[g + 1] - row_off[g]) / (BK * EPB);
-    ti.a_kb0 = ti.b_kb0 = row_off[g] / (BK * EPB);
+    ti.kb_count = (prow_off[g + 1] - prow_off[g]) / (BK * EPB);
+    ti.a_kb0 = ti.b_kb0 = prow_off[g] / (BK * EPB);
     ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
@@ -698,6 +711,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
+  int32_t* prow_off = tile_off + (p.G + 1);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   const uint32_t smem_base = smem_u32(smem);
@@ -729,7 +743,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
     tmem_alloc_pair(smem_u32(tmem_base_s), Cfg::kTmemCols);
     tmem_relinquish_pair();
   }
-  if (warp == 1) build_group_tables(p, row_off, tile_off, lane, true, Cfg::BN);
+  if (warp == 1) build_group_tables(p, row_off, prow_off, tile_off, lane, true, Cfg::BN);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the even CTA's barriers exist before the odd CTA's copies signal them
@@ -752,9 +766,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, rank);
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, rank);
         const int32_t b_half = static_cast<int32_t>(ti.b_row + 128 * rank);
-        const int32_t a_band = static_cast<int32_t>(ti.a_row >> 7);
+        const int32_t a_band = static_cast<int32_t>(ti.a_sf_row >> 7);
         const int32_t b_band = static_cast<int32_t>(ti.b_row >> 7);
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -799,7 +813,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, 0);
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, 0);
         if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
@@ -853,7 +867,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       const int j = static_cast<int>(warp - kFirstSfWarp);
       uint32_t stage = 0, phase = 0;
       for (int64_t t = unit0; t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, 0);
+        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, 0);
         bool ok = true;
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           // the stage's previous MMAs finished before its producer refilled it
@@ -900,7 +914,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
     const uint32_t tempty_even = mapa_shared(tempty_bar, 0);
     uint32_t acc_phase = 0;
     for (int64_t t = unit0; t < total_units; t += ustride) {
-      const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, tile_off, rank);
+      const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, rank);
       if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -1020,8 +1034,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
                                 int num_sms, int tile_n, int pair, int bk, int prefetch,
-                                int inject, uint64_t timeout_ns, cudaStream_t stream) {
+                                int inject, uint64_t timeout_ns, int unaligned,
+                                cudaStream_t stream) {
   GemmParams p;
+  p.unaligned = unaligned;
   p.prefetch = prefetch;
   p.inject = inject;
   p.timeout_ns = timeout_ns;
@@ -1045,10 +1061,14 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   // operand geometry: rows x contraction length (elements) of A and B
   //   fprop: A [M_cap, K], B [G*N, K];  wgrad: A [N, M_cap], B [K, M_cap];
   //   dgrad: A [M_cap, N], B [K, G*N]  (the transposed weight copy)
+  // With unaligned groups the colwise copies and A's scales are padded per
+  // group: M_pad = M_cap + 128 G rows replace M_cap there.
+  const int64_t M_pad = unaligned ? M_cap + 128 * static_cast<int64_t>(G) : M_cap;
   const int64_t a_rows = mode == 0 ? M_cap : (mode == 1 ? N : M_cap);
   const int64_t b_rows = mode == 0 ? G * N : K;
-  const int64_t a_kdim = mode == 0 ? K : (mode == 1 ? M_cap : N);
-  const int64_t b_kdim = mode == 0 ? K : (mode == 1 ? M_cap : G * N);
+  const int64_t a_kdim = mode == 0 ? K : (mode == 1 ? M_pad : N);
+  const int64_t b_kdim = mode == 0 ? K : (mode == 1 ? M_pad : G * N);
+  const int64_t a_sf_rows = mode == 1 ? a_rows : M_pad;  // rows of A's scale matrix
   const int64_t blk = nvfp4 ? 16 : 32;
   p.a_atoms_row = a_kdim / blk / 4;
   p.b_atoms_row = b_kdim / blk / 4;
@@ -1064,7 +1084,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
 
   // default: the CTA-pair kernel (256 x 256 units) whenever a stage is 128
   // bytes of K and B spans at least the two 128-row bands of one unit
-  if (tile_n == 0 && !pair && BKB == 128 && b_rows >= 256) {
+  if (unaligned && !(BKB == 128 && b_rows >= 256 && !nvfp4)) return cudaErrorInvalidValue;
+  if (unaligned || (tile_n == 0 && !pair && BKB == 128 && b_rows >= 256)) {
     CUtensorMap ta, tb, tsa, tsb;
     const int atoms = nvfp4 ? 4 : 1;  // scale tiles along K per stage and band
     const uint64_t b_bands = static_cast<uint64_t>(b_rows / 128);
@@ -1075,7 +1096,7 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
     if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows, 128, 128) ||
         !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows, 128, 128) ||
         !make_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128,
-                      static_cast<uint64_t>((a_rows / 128) * p.a_atoms_row), 512, 128,
+                      static_cast<uint64_t>((a_sf_rows / 128) * p.a_atoms_row), 512, 128,
                       static_cast<uint32_t>(atoms), CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, b_sf, sfb_dims, sfb_strides, sfb_box))
       return cudaErrorInvalidValue;

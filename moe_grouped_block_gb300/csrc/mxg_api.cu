@@ -11,11 +11,11 @@
 namespace mxg {
 cudaError_t launch_group_offsets(const void* sizes, int is_int64, int G, int64_t mult,
                                  int64_t last_dim, int64_t cap, int64_t* ws, int32_t* status,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int round128);
 cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q_row, uint8_t* sf_row,
                                   uint8_t* q_col, uint8_t* sf_col, int32_t* status, int num_sms,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, bool unaligned);
 cudaError_t launch_nvfp4_quantize(const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q, uint8_t* sf,
                                   float* outer, int32_t* status, int num_sms, cudaStream_t stream);
@@ -32,7 +32,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
                                 int num_sms, int tile_n, int pair, int bk, int prefetch,
-                                int inject, uint64_t timeout_ns, cudaStream_t stream);
+                                int inject, uint64_t timeout_ns, int unaligned,
+                                cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -121,7 +122,55 @@ mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int
   if (st != MXG_OK) return st;
   return launched(mxg::launch_group_offsets(sizes, sizes_is_int64 ? 1 : 0, G, multiplier, last_dim,
                                             rows_capacity, ws, dev_status,
-                                            reinterpret_cast<cudaStream_t>(stream)),
+                                            reinterpret_cast<cudaStream_t>(stream), 1),
+                  1);
+}
+
+mxg_status_t mxg_group_offsets_unaligned(const void* sizes, int sizes_is_int64, int G,
+                                         int64_t multiplier, int64_t last_dim,
+                                         int64_t rows_capacity, int64_t* ws, int32_t* dev_status,
+                                         mxg_stream_t stream) {
+  if (sizes == nullptr || ws == nullptr || G < 1 || G > 65536 || multiplier < 1 || last_dim < 1 ||
+      rows_capacity < 0)
+    return MXG_ERR_INVALID_ARG;
+  int sms = 0;
+  const mxg_status_t st = current_device(&sms);
+  if (st != MXG_OK) return st;
+  return launched(mxg::launch_group_offsets(sizes, sizes_is_int64 ? 1 : 0, G, multiplier, last_dim,
+                                            rows_capacity, ws, dev_status,
+                                            reinterpret_cast<cudaStream_t>(stream), 0),
+                  1);
+}
+
+int64_t mxg_unaligned_rows_capacity(int64_t rows_capacity, int G) {
+  if (rows_capacity < 0 || G < 1) return 0;
+  return rows_capacity + 128 * static_cast<int64_t>(G);
+}
+
+mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
+                                          int64_t rows_capacity, int64_t cols,
+                                          const int64_t* group_ws, int G, uint8_t* q_row,
+                                          uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                                          int32_t* dev_status, mxg_stream_t stream) {
+  if (x == nullptr || group_ws == nullptr || G < 1 || G > 1024) return MXG_ERR_INVALID_ARG;
+  if (layout != MXG_ROWWISE && layout != MXG_COLWISE && layout != MXG_BOTH)
+    return MXG_ERR_INVALID_ARG;
+  const bool row = (layout & MXG_ROWWISE) != 0, col = (layout & MXG_COLWISE) != 0;
+  if ((row && (q_row == nullptr || sf_row == nullptr)) ||
+      (col && (q_col == nullptr || sf_col == nullptr)))
+    return MXG_ERR_INVALID_ARG;
+  if (!mult128(rows_capacity) || !mult128(cols) || cols == 0) return MXG_ERR_ALIGNMENT;
+  if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(sf_row))) ||
+      (col && (!aligned16(q_col) || !aligned16(sf_col))))
+    return MXG_ERR_ALIGNMENT;
+  int sms = 0;
+  const mxg_status_t st = current_device(&sms);
+  if (st != MXG_OK) return st;
+  if (rows_capacity == 0) return MXG_OK;
+  return launched(mxg::launch_mxfp8_quantize(row, col, static_cast<const uint16_t*>(x),
+                                             rows_capacity, cols, group_ws, G, q_row, sf_row,
+                                             q_col, sf_col, dev_status, sms,
+                                             reinterpret_cast<cudaStream_t>(stream), true),
                   1);
 }
 
@@ -160,7 +209,7 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
                                                rows_capacity, cols, group_ws, G,
                                                static_cast<uint8_t*>(q_row), sf_row,
                                                static_cast<uint8_t*>(q_col), sf_col, dev_status,
-                                               sms, s),
+                                               sms, s, false),
                     1);
   if (row) {
     const mxg_status_t r = launched(
@@ -183,7 +232,8 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
                                       int64_t K, const float* alpha, const float* beta,
                                       const float* bias, void* C, mxg_out_t out_type,
                                       int32_t* dev_status, int inject,
-                                      uint64_t timeout_ns, mxg_stream_t stream) {
+                                      uint64_t timeout_ns, mxg_stream_t stream,
+                                      int unaligned) {
   if (A == nullptr || B == nullptr || C == nullptr || group_ws == nullptr || G < 1 || G > 1024)
     return MXG_ERR_INVALID_ARG;
   if (fmt != MXG_MXFP8_E4M3 && fmt != MXG_NVFP4_ROWSCALED) return MXG_ERR_INVALID_ARG;
@@ -196,6 +246,9 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   if (nv && (mode == MXG_DGRAD_NN || beta != nullptr || A->outer == nullptr || B->outer == nullptr))
     return MXG_ERR_INVALID_ARG;  // row-scaled NVFP4: fprop and wgrad, no beta
   if (bias != nullptr && mode == MXG_WGRAD_NT) return MXG_ERR_INVALID_ARG;
+  // unaligned groups: MXFP8 on the CTA-pair kernel, whose B spans >= 256 rows
+  if (unaligned && (nv || (mode == MXG_FPROP_TN ? N * static_cast<int64_t>(G) : K) < 256))
+    return MXG_ERR_INVALID_ARG;
   if (!mult128(M_cap) || !mult128(N) || !mult128(K) || N == 0 || K == 0)
     return MXG_ERR_ALIGNMENT;
 
@@ -212,7 +265,7 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
                       out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), env_pair(),
                       env_bk(), env_prefetch(), inject,
-                      timeout_ns, reinterpret_cast<cudaStream_t>(stream)),
+                      timeout_ns, unaligned, reinterpret_cast<cudaStream_t>(stream)),
                   1);
 }
 
@@ -225,7 +278,7 @@ mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_
   (void)workspace;
   (void)workspace_bytes;
   return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                           out_type, dev_status, 0, mxg::kDefaultWaitNs, stream);
+                           out_type, dev_status, 0, mxg::kDefaultWaitNs, stream, 0);
 }
 
 mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
@@ -238,7 +291,17 @@ mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, cons
   const uint64_t t = wait_timeout_ns == 0 ? mxg::kDefaultWaitNs
                                           : static_cast<uint64_t>(wait_timeout_ns);
   return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                           out_type, dev_status, inject_flags, t, stream);
+                           out_type, dev_status, inject_flags, t, stream, 0);
+}
+
+mxg_status_t mxg_grouped_gemm_unaligned(mxg_gemm_mode_t mode, const mxg_operand_t* A,
+                                        const mxg_operand_t* B, const int64_t* group_ws, int G,
+                                        int64_t M_cap, int64_t N, int64_t K, const float* alpha,
+                                        const float* beta, const float* bias, void* C,
+                                        mxg_out_t out_type, int32_t* dev_status,
+                                        mxg_stream_t stream) {
+  return grouped_gemm_impl(MXG_MXFP8_E4M3, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias,
+                           C, out_type, dev_status, 0, mxg::kDefaultWaitNs, stream, 1);
 }
 
 size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,

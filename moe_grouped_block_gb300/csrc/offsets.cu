@@ -9,7 +9,8 @@
 //
 // Sanitisation (this library's contract, recorded in the status word): a
 // negative size counts as 0, a size that is not a multiple of 128 is rounded
-// down, and rows past rows_capacity are dropped.  With P_g the running sum
+// down (unless round128 is 0: the unaligned-group entry points keep every
+// size), and rows past rows_capacity are dropped.  With P_g the running sum
 // of the (non-negative, rounded) sizes, the kept prefix is min(P_g, cap), so
 // the kept size of group g is min(P_{g+1}, cap) - min(P_g, cap).
 #include "mxg_device.cuh"
@@ -18,7 +19,8 @@ namespace mxg {
 
 __global__ void __launch_bounds__(32, 1)
     group_offsets_kernel(const void* __restrict__ sizes, int is_int64, int G, int64_t mult,
-                         int64_t last_dim, int64_t cap, int64_t* __restrict__ ws, int32_t* status) {
+                         int64_t last_dim, int64_t cap, int64_t* __restrict__ ws, int32_t* status,
+                         int round128) {
   const uint32_t lane = threadIdx.x;
   int64_t carry = 0;  // unclamped running sum before this round
   int32_t bits = 0;
@@ -34,7 +36,7 @@ __global__ void __launch_bounds__(32, 1)
         bits |= MXG_DEV_NEG_SIZE;
         s = 0;
       }
-      if (s & 127) {
+      if (round128 && (s & 127)) {
         bits |= MXG_DEV_MISALIGNED;
         s &= ~static_cast<int64_t>(127);
       }
@@ -65,8 +67,9 @@ __global__ void __launch_bounds__(32, 1)
 
 cudaError_t launch_group_offsets(const void* sizes, int is_int64, int G, int64_t mult,
                                  int64_t last_dim, int64_t cap, int64_t* ws, int32_t* status,
-                                 cudaStream_t stream) {
-  group_offsets_kernel<<<1, 32, 0, stream>>>(sizes, is_int64, G, mult, last_dim, cap, ws, status);
+                                 cudaStream_t stream, int round128) {
+  group_offsets_kernel<<<1, 32, 0, stream>>>(sizes, is_int64, G, mult, last_dim, cap, ws, status,
+                                             round128);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,71 @@ __device__ __forceinline__ int64_t live_rows_warp(const int64_t* ws, int G, int6
   return sum;
 }
 
+// Unaligned groups: one warp builds row_off (data rows: sizes taken as
+// non-negative, the running sum capped at cap), prow_off (each kept size
+// rounded up to 128: the padded row where the group's scales and colwise slab
+// start) and tile_off (128-row tiles per group, prefix) in shared memory.
+__device__ __forceinline__ void unaligned_tables_warp(const int64_t* ws, int G, int64_t cap,
+                                                      int32_t* row_off, int32_t* prow_off,
+                                                      int32_t* tile_off, int32_t* status) {
+  const uint32_t lane = lane_id();
+  auto scan = [&](int64_t v) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t u = __shfl_up_sync(0xFFFFFFFFu, v, d);
+      if (lane >= static_cast<uint32_t>(d)) v += u;
+    }
+    return v;
+  };
+  int64_t carry = 0, carry_pad = 0;
+  int32_t bits = 0;
+  for (int base = 0; base < G; base += 32) {
+    const int g = base + static_cast<int>(lane);
+    int64_t s = 0;
+    if (g < G) {
+      s = ws[g];
+      if (s < 0) {
+        s = 0;
+        bits |= MXG_DEV_NEG_SIZE;
+      }
+      if (s > cap) s = cap;
+    }
+    const int64_t incl = scan(s);
+    const int64_t before = min(carry + incl - s, cap), after = min(carry + incl, cap);
+    if (carry + incl > cap && s > 0) bits |= MXG_DEV_SUM_OVER_CAPACITY;
+    const int64_t pad = ((after - before) + 127) & ~static_cast<int64_t>(127);
+    const int64_t pincl = scan(pad);
+    if (g < G) {
+      row_off[g] = static_cast<int32_t>(before);
+      prow_off[g] = static_cast<int32_t>(carry_pad + pincl - pad);
+      tile_off[g] = static_cast<int32_t>((carry_pad + pincl - pad) >> 7);
+    }
+    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    carry_pad += __shfl_sync(0xFFFFFFFFu, pincl, 31);
+  }
+  if (lane == 0) {
+    row_off[G] = static_cast<int32_t>(min(carry, cap));
+    prow_off[G] = static_cast<int32_t>(carry_pad);
+    tile_off[G] = static_cast<int32_t>(carry_pad >> 7);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, d);
+  if (lane == 0 && blockIdx.x == 0) status_set(status, bits);
+}
+
+// Largest g with tile_off[g] <= rt (binary search over G + 1 entries).
+__device__ __forceinline__ int group_of_tile(const int32_t* tile_off, int G, int64_t rt) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_off[mid] <= rt)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
 // Scaled bf16 pair (already multiplied by 2^-e, exact) -> two E4M3 bytes.
 __device__ __forceinline__ uint32_t e4m3_pair(uint32_t w) { return cvt_e4m3x2(bf16lo(w), bf16hi(w)); }
 
@@ -90,16 +155,23 @@ __device__ __forceinline__ float abs_hi(uint32_t m) { return __uint_as_float(m &
 }  // namespace
 
 // Shared memory: two 32 KB bf16 tiles (TMA double buffer), two 512-byte scale
-// staging tiles, two mbarriers, the live-row count and the abort flag.
+// staging tiles, two mbarriers, the live-row count and the abort flag; with
+// unaligned groups, three int32 tables of G + 1 entries after them.
 constexpr int kQTileBytes = 128 * 128 * 2;
 constexpr int kQSmemBytes = 2 * kQTileBytes + 2 * 512 + 2 * 8 + 16 + 1024;
 
-template <bool ROW, bool COL>
-__global__ void __launch_bounds__(256, 3)
+// UNA: group sizes of any value.  Tiles are then 128-row tiles of each group
+// (the last one may extend past the group: those rows are zeroed in shared
+// memory after the load), written densely to q_row but at the group's padded
+// row offset in sf_row, q_col and sf_col; cap_col is the row count of the
+// colwise copy (cap, or cap + 128 G when padded).
+template <bool ROW, bool COL, bool UNA>
+__global__ void __launch_bounds__(256, UNA ? 2 : 3)
     mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                           const int64_t* __restrict__ group_ws, int G, uint8_t* __restrict__ q_row,
                           uint8_t* __restrict__ sf_row, uint8_t* __restrict__ q_col,
-                          uint8_t* __restrict__ sf_col, int qcol_v8, int32_t* status) {
+                          uint8_t* __restrict__ sf_col, int qcol_v8, int64_t cap_col,
+                          int32_t* status) {
   extern __shared__ uint8_t qsmem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -108,6 +180,9 @@ __global__ void __launch_bounds__(256, 3)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sfc_s + 512);
   int64_t* live_s = reinterpret_cast<int64_t*>(bars + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(live_s + 1);
+  int32_t* row_off = reinterpret_cast<int32_t*>(live_s + 2);  // UNA only
+  int32_t* prow_off = row_off + (G + 1);
+  int32_t* tile_off = prow_off + (G + 1);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   if (threadIdx.x == 0) {
@@ -117,19 +192,45 @@ __global__ void __launch_bounds__(256, 3)
     fence_barrier_init();
   }
   if (warp == 0) {
-    const int64_t l = live_rows_warp(group_ws, G, cap, status);
-    if (lane == 0) *live_s = l;
+    if (UNA) {
+      unaligned_tables_warp(group_ws, G, cap, row_off, prow_off, tile_off, status);
+      if (lane == 0) *live_s = 0;
+    } else {
+      const int64_t l = live_rows_warp(group_ws, G, cap, status);
+      if (lane == 0) *live_s = l;
+    }
   }
   __syncthreads();
   const int64_t kt = cols >> 7;
-  const int64_t tiles = (*live_s >> 7) * kt;
+  const int64_t row_tiles = UNA ? static_cast<int64_t>(tile_off[G]) : (*live_s >> 7);
+  const int64_t tiles = row_tiles * kt;
+  // row tile rt -> first data row, first padded row, rows of the group in it
+  struct RowTile {
+    int64_t m0, mp;
+    int valid;
+  };
+  auto row_tile = [&](int64_t rt) {
+    RowTile r;
+    if (UNA) {
+      const int g = group_of_tile(tile_off, G, rt);
+      const int64_t i = rt - tile_off[g];
+      r.m0 = row_off[g] + 128 * i;
+      r.mp = prow_off[g] + 128 * i;
+      const int64_t left = row_off[g + 1] - r.m0;
+      r.valid = static_cast<int>(left < 128 ? left : 128);
+    } else {
+      r.m0 = r.mp = rt << 7;
+      r.valid = 128;
+    }
+    return r;
+  };
 
   // thread 0 issues the TMA load of tile t into buffer b
   auto issue = [&](int64_t t, int b) {
     const uint32_t bar = smem_u32(&bars[b]);
     mbar_arrive_expect_tx(bar, kQTileBytes);
     tma_load_2d(smem_u32(sm + b * kQTileBytes), &tmap_x, bar, static_cast<int32_t>((t % kt) << 7),
-                static_cast<int32_t>((t / kt) << 7));
+                static_cast<int32_t>(row_tile(t / kt).m0));
   };
   if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
     prefetch_tmap(&tmap_x);
@@ -153,8 +254,17 @@ __global__ void __launch_bounds__(256, 3)
     __syncthreads();
     if (*abort_flag) break;
 
-    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
+    const RowTile rtl = row_tile(t / kt);
+    const int64_t m0 = rtl.m0, mp = rtl.mp, k0 = (t % kt) << 7;
     const uint32_t* tile = reinterpret_cast<const uint32_t*>(sm + b * kQTileBytes);
+    if (UNA && rtl.valid < 128) {
+      // rows past the group: zeros (their scales come out 0, their colwise
+      // bytes are the padding); ordered before the buffer's next TMA write
+      uint32_t* wt = reinterpret_cast<uint32_t*>(sm + b * kQTileBytes);
+      for (int w = rtl.valid * 64 + static_cast<int>(threadIdx.x); w < 128 * 64; w += 256) wt[w] = 0;
+      fence_proxy_async_shared();
+      __syncthreads();
+    }
 
     // ---- phase 1: rows (16 lanes per row, 16-byte chunks; conflict-free per 8-lane phase)
     if (ROW) {
@@ -169,7 +279,8 @@ __global__ void __launch_bounds__(256, 3)
         const int e = mx_exponent(a);
         const uint32_t sb = bf16_pow2_neg_bits(e);
         const uint2 o = quant8(v, sb | (sb << 16));
-        *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
+        if (!UNA || static_cast<int>(r) < rtl.valid)
+          *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
         if ((cl & 3u) == 0)
           sfr_s[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
       }
@@ -198,8 +309,8 @@ __global__ void __launch_bounds__(256, 3)
         olo[i] = cvt_e4m3x2(bf16lo(u0), bf16lo(u1)) | (cvt_e4m3x2(bf16lo(u2), bf16lo(u3)) << 16);
         ohi[i] = cvt_e4m3x2(bf16hi(u0), bf16hi(u1)) | (cvt_e4m3x2(bf16hi(u2), bf16hi(u3)) << 16);
       }
-      uint8_t* dlo = q_col + (k0 + 2 * cp) * cap + m0 + 32 * j;
-      uint8_t* dhi = dlo + cap;
+      uint8_t* dlo = q_col + (k0 + 2 * cp) * cap_col + mp + 32 * j;
+      uint8_t* dhi = dlo + cap_col;
       if (qcol_v8) {
         st_global_32B(dlo, olo);
         st_global_32B(dhi, ohi);
@@ -216,12 +327,12 @@ __global__ void __launch_bounds__(256, 3)
     __syncthreads();
     if (threadIdx.x < 32) {
       if (ROW) {
-        const int64_t atom = (m0 >> 7) * kt + (k0 >> 7);
+        const int64_t atom = (mp >> 7) * kt + (k0 >> 7);
         reinterpret_cast<uint4*>(sf_row + atom * 512)[threadIdx.x] =
             reinterpret_cast<const uint4*>(sfr_s)[threadIdx.x];
       }
     } else if (COL && threadIdx.x < 64) {
-      const int64_t atom = (k0 >> 7) * (cap >> 7) + (m0 >> 7);
+      const int64_t atom = (k0 >> 7) * (cap_col >> 7) + (mp >> 7);
       reinterpret_cast<uint4*>(sf_col + atom * 512)[threadIdx.x - 32] =
           reinterpret_cast<const uint4*>(sfc_s)[threadIdx.x - 32];
     }
@@ -237,31 +348,39 @@ __global__ void __launch_bounds__(256, 3)
       }
 }
 
+// unaligned: group sizes of any value (group_ws required); the colwise copy
+// and the scales are then padded per group (cap + 128 G rows).
 cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q_row, uint8_t* sf_row,
                                   uint8_t* q_col, uint8_t* sf_col, int32_t* status, int num_sms,
-                                  cudaStream_t stream) {
-  const int64_t max_tiles = (cap >> 7) * (cols >> 7);
+                                  cudaStream_t stream, bool unaligned) {
+  const int64_t cap_col = unaligned ? cap + 128 * static_cast<int64_t>(G) : cap;
+  const int64_t max_tiles = (cap_col >> 7) * (cols >> 7);
   if (max_tiles == 0) return cudaSuccess;
   CUtensorMap tm;
   if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, static_cast<uint64_t>(cols),
                     static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 128, 128,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  const int64_t per_sm = 3;
+  const int smem = kQSmemBytes + (unaligned ? 12 * (G + 1) + 16 : 0);
+  const int64_t per_sm = smem <= 75 * 1024 ? 3 : 2;
   const int grid = static_cast<int>(max_tiles < num_sms * per_sm ? max_tiles : num_sms * per_sm);
   auto launch = [&](auto kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kQSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int qcol_v8 = (reinterpret_cast<uintptr_t>(q_col) & 31u) == 0 ? 1 : 0;
-    kern<<<grid, 256, kQSmemBytes, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col,
-                                              sf_col, qcol_v8, status);
+    kern<<<grid, 256, smem, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col, sf_col,
+                                       qcol_v8, cap_col, status);
     return cudaGetLastError();
   };
-  if (row && col) return launch(mxfp8_quantize_kernel<true, true>);
-  if (row) return launch(mxfp8_quantize_kernel<true, false>);
-  return launch(mxfp8_quantize_kernel<false, true>);
+  if (unaligned) {
+    if (row && col) return launch(mxfp8_quantize_kernel<true, true, true>);
+    if (row) return launch(mxfp8_quantize_kernel<true, false, true>);
+    return launch(mxfp8_quantize_kernel<false, true, true>);
+  }
+  if (row && col) return launch(mxfp8_quantize_kernel<true, true, false>);
+  if (row) return launch(mxfp8_quantize_kernel<true, false, false>);
+  return launch(mxfp8_quantize_kernel<false, true, false>);
 }
 
 }  // namespace mxg

@@ -82,6 +82,17 @@ def load() -> ctypes.CDLL:
         L.mxg_version.argtypes = []
         L.mxg_launch_count.restype = ctypes.c_uint64
         L.mxg_launch_count.argtypes = []
+        L.mxg_unaligned_rows_capacity.restype = i64
+        L.mxg_unaligned_rows_capacity.argtypes = [i64, c_int]
+        L.mxg_group_offsets_unaligned.restype = c_int
+        L.mxg_group_offsets_unaligned.argtypes = [vp, c_int, c_int, i64, i64, i64, vp, vp, vp]
+        L.mxg_group_quantize_unaligned.restype = c_int
+        L.mxg_group_quantize_unaligned.argtypes = [c_int, vp, i64, i64, vp, c_int, vp, vp, vp, vp,
+                                                   vp, vp]
+        L.mxg_grouped_gemm_unaligned.restype = c_int
+        L.mxg_grouped_gemm_unaligned.argtypes = [c_int, ctypes.POINTER(Operand),
+                                                 ctypes.POINTER(Operand), vp, c_int, i64, i64, i64,
+                                                 vp, vp, vp, vp, c_int, vp, vp]
         _lib = L
     return _lib
 
@@ -178,6 +189,43 @@ def mxg_dequantize(fmt: int, layout: int, q, sf, outer, rows: int, cols: int, ou
                                  out_type, _s(stream)))
 
 
+def mxg_unaligned_rows_capacity(rows_capacity: int, G: int) -> int:
+    return load().mxg_unaligned_rows_capacity(rows_capacity, G)
+
+
+def mxg_group_offsets_unaligned(sizes: torch.Tensor, multiplier: int, last_dim: int,
+                                rows_capacity: int, ws: torch.Tensor,
+                                dev_status: torch.Tensor | None = None, stream=None) -> None:
+    assert sizes.dtype in (torch.int32, torch.int64) and ws.dtype == torch.int64
+    _check("mxg_group_offsets_unaligned",
+           load().mxg_group_offsets_unaligned(_p(sizes), 1 if sizes.dtype == torch.int64 else 0,
+                                              sizes.numel(), multiplier, last_dim, rows_capacity,
+                                              _p(ws), _p(dev_status), _s(stream)))
+
+
+def mxg_group_quantize_unaligned(layout: int, x: torch.Tensor, rows_capacity: int, cols: int,
+                                 group_ws: torch.Tensor, G: int, q_row=None, sf_row=None,
+                                 q_col=None, sf_col=None, dev_status=None, stream=None) -> None:
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    _check("mxg_group_quantize_unaligned",
+           load().mxg_group_quantize_unaligned(layout, _p(x), rows_capacity, cols, _p(group_ws), G,
+                                               _p(q_row), _p(sf_row), _p(q_col), _p(sf_col),
+                                               _p(dev_status), _s(stream)))
+
+
+def mxg_grouped_gemm_unaligned(mode: int, A: tuple, B: tuple, group_ws: torch.Tensor, G: int,
+                               M_cap: int, N: int, K: int, alpha=None, beta=None, C=None,
+                               out_type: int = MXG_OUT_F32, dev_status=None, stream=None,
+                               bias=None) -> None:
+    """A, B: (data, scale) device tensors (MXFP8)."""
+    a = Operand(_p(A[0]), _p(A[1]), None)
+    b = Operand(_p(B[0]), _p(B[1]), None)
+    _check("mxg_grouped_gemm_unaligned",
+           load().mxg_grouped_gemm_unaligned(mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws),
+                                             G, M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C),
+                                             out_type, _p(dev_status), _s(stream)))
+
+
 def mxg_status_string(code: int) -> str:
     return load().mxg_status_string(code).decode()
 
@@ -203,6 +251,21 @@ def alloc_mxfp8(rows: int, cols: int, rowwise=True, colwise=False, device="cuda"
     if colwise:
         out["q_col"] = torch.empty((cols, rows), dtype=torch.uint8, device=device)
         out["sf_col"] = torch.empty(rows * cols // 32, dtype=torch.uint8, device=device)
+    return out
+
+
+def alloc_mxfp8_unaligned(rows: int, cols: int, G: int, rowwise=True, colwise=False,
+                          device="cuda") -> dict:
+    """Buffers for mxg_group_quantize_unaligned: dense rowwise data, scales and
+    colwise copy over the padded row count rows + 128 G."""
+    rp = rows + 128 * G
+    out = {}
+    if rowwise:
+        out["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=device)
+        out["sf_row"] = torch.empty(rp * cols // 32, dtype=torch.uint8, device=device)
+    if colwise:
+        out["q_col"] = torch.empty((cols, rp), dtype=torch.uint8, device=device)
+        out["sf_col"] = torch.empty(rp * cols // 32, dtype=torch.uint8, device=device)
     return out
 
 

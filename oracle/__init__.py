@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             L.mxg_oracle_swizzle.argtypes = [c_p, i64, i64, c_p]
             L.mxg_oracle_group_offsets.restype = i32
             L.mxg_oracle_group_offsets.argtypes = [c_p, ctypes.c_int, i64, i64, i64, c_p]
+            L.mxg_oracle_group_offsets_unaligned.restype = i32
+            L.mxg_oracle_group_offsets_unaligned.argtypes = [c_p, ctypes.c_int, i64, i64, i64, c_p]
             L.mxg_oracle_mxfp8_quantize_rowwise.argtypes = [c_p, i64, i64, c_p, c_p]
             L.mxg_oracle_mxfp8_quantize_colwise.argtypes = [c_p, i64, i64, i64, c_p, c_p]
             L.mxg_oracle_nvfp4_quantize_rowwise.argtypes = [c_p, i64, i64, c_p, c_p, c_p]
@@ -413,3 +415,148 @@ def grouped_gemm_dgrad(a: dict, b_t: dict, group_rows, G: int, N: int, K: int, a
             res = res + be[g] * np.asarray(c_in, np.float64)[np.ix_(rows[sel], cols)]
         out[sel] = res
     return rows, cols, out
+
+
+# --------------------------------------------------------------------------
+# groups of any size (MXFP8): each group is its own tensor, zero-padded to a
+# multiple of 128 rows.  TransformerEngine gemm.py grouped_gemm: padding is
+# part of a group and filled with zeros so that it does not change the
+# result; gemm.py apply_padding_to_scale_inv pads scale matrices of non-128
+# dims; PR #2763 review thread: the 128-row rule comes from the offset
+# arithmetic of the grouped quantize and GEMM setup.  Everything below is
+# composed from the aligned (pinned) quantizer, dequantizer and swizzle.
+# --------------------------------------------------------------------------
+def group_offsets_unaligned(sizes, multiplier: int, last_dim: int, rows_capacity: int):
+    """As group_offsets, with sizes kept as given (no rounding to 128)."""
+    s = np.ascontiguousarray(np.asarray(sizes).astype(np.int64))
+    G = s.size
+    ws = np.zeros(2 * G + 1, np.int64)
+    st = lib().mxg_oracle_group_offsets_unaligned(_ptr(s), G, multiplier, last_dim,
+                                                  rows_capacity, _ptr(ws))
+    return ws, int(st)
+
+
+def padded_rows(ws: np.ndarray, G: int) -> np.ndarray:
+    """Padded row offsets [G+1]: prefix sums of each group's rows rounded up to 128."""
+    sizes = np.asarray(ws[:G], np.int64)
+    return np.concatenate([[0], np.cumsum((sizes + 127) // 128 * 128)]).astype(np.int64)
+
+
+def unaligned_rows_capacity(rows_capacity: int, G: int) -> int:
+    return rows_capacity + 128 * G
+
+
+def mxfp8_quantize_unaligned(x, ws: np.ndarray, G: int, rows_capacity: int, rowwise=True,
+                             colwise=False, fill: int = 0):
+    """MXFP8 quantize of each group of bf16 x[rows_capacity, cols] as its own
+    tensor zero-padded to P_g = ceil128(M_g) rows.  Outputs (pre-filled with
+    ``fill`` where nothing is written):
+      q_row  [rows_capacity, cols] dense (group g at its data rows);
+      sf_row swizzled [R_pad, cols/32], group g's scale rows at its padded offset;
+      q_col  [cols, R_pad] and sf_col swizzled [cols, R_pad/32], group g's slab at
+      its padded offset;   R_pad = rows_capacity + 128 G."""
+    xu = _u16(x)
+    R, cols = xu.shape
+    assert R == rows_capacity and cols % 128 == 0 and R % 128 == 0
+    offs = live_rows(ws, G)
+    poffs = padded_rows(ws, G)
+    Rp = unaligned_rows_capacity(R, G)
+    C = cols // 32
+    out = {}
+    q_row = np.full((R, cols), fill, np.uint8)
+    sfp_row = np.full((Rp, C), fill, np.uint8)
+    q_col = np.full((cols, Rp), fill, np.uint8)
+    sfp_col = np.full((cols, Rp // 32), fill, np.uint8)
+    for g in range(G):
+        m, lo, plo = int(ws[g]), int(offs[g]), int(poffs[g])
+        if m == 0:
+            continue
+        P = (m + 127) // 128 * 128
+        slab = np.zeros((P, cols), np.uint16)
+        slab[:m] = xu[lo:lo + m]
+        qs = mxfp8_quantize(slab, P, P, rowwise=rowwise, colwise=colwise)
+        if rowwise:
+            q_row[lo:lo + m] = qs["q_row"][:m]
+            sfp_row[plo:plo + P] = unswizzle(qs["sf_row"], P, C)
+        if colwise:
+            q_col[:, plo:plo + P] = qs["q_col"]
+            sfp_col[:, plo // 32:(plo + P) // 32] = unswizzle(qs["sf_col"], cols, P // 32)
+    if rowwise:
+        out["q_row"], out["sf_row"] = q_row, swizzle(sfp_row)
+    if colwise:
+        out["q_col"], out["sf_col"] = q_col, swizzle(sfp_col)
+    return out
+
+
+def _padded_rowwise(a: dict, ws: np.ndarray, G: int, cols: int) -> np.ndarray:
+    """Dense rowwise data moved to the padded rows of its scales (zero rows
+    in the padding), so that dequantize_rows reads data and scales alike."""
+    offs, poffs = live_rows(ws, G), padded_rows(ws, G)
+    q_pad = np.zeros((int(poffs[-1]) + 128, cols), np.uint8)
+    for g in range(G):
+        m = int(ws[g])
+        q_pad[poffs[g]:poffs[g] + m] = a["q"][offs[g]:offs[g] + m]
+    return q_pad
+
+
+def grouped_gemm_fprop_unaligned(a: dict, b: dict, ws: np.ndarray, G: int, N: int, K: int,
+                                 alpha=None, beta=None, c_in=None, bias=None):
+    """fprop TN (MXFP8) for groups of any size: a = {"q": dense rowwise data
+    [M_cap, K], "sf": padded swizzled scales}.  Returns (rows, [rows, N])
+    over the live data rows; the per-group product is as in grouped_gemm_fprop."""
+    offs, poffs = live_rows(ws, G), padded_rows(ws, G)
+    q_pad = _padded_rowwise(a, ws, G, K)
+    al = _per_group(alpha, G)
+    be = np.zeros(G) if beta is None else np.asarray(beta, np.float64).reshape(G)
+    rows = np.arange(offs[-1])
+    out = np.zeros((rows.size, N), np.float64)
+    for g in range(G):
+        m = int(ws[g])
+        if m == 0:
+            continue
+        A = dequantize_rows("mxfp8", q_pad, a["sf"], K, poffs[g] + np.arange(m))
+        B = dequantize_rows("mxfp8", b["q"], b["sf"], K, g * N + np.arange(N))
+        res = al[g] * (A @ B.T)
+        if bias is not None:
+            res = res + np.asarray(bias, np.float64)[g][None, :]
+        r = offs[g] + np.arange(m)
+        if c_in is not None and be[g] != 0.0:
+            res = res + be[g] * np.asarray(c_in, np.float64)[r]
+        out[r] = res
+    return rows, out
+
+
+def grouped_gemm_wgrad_unaligned(a_t: dict, b_t: dict, ws: np.ndarray, G: int, M_cap: int,
+                                 N: int, K: int, alpha=None, beta=None, c_in=None):
+    """wgrad NT (MXFP8) for groups of any size: the colwise copies are padded
+    per group, so each group contracts over its padded slab (zeros add
+    nothing) -- grouped_gemm_wgrad over the padded offsets."""
+    poffs = padded_rows(ws, G)
+    return grouped_gemm_wgrad(a_t, b_t, poffs, unaligned_rows_capacity(M_cap, G), N, K,
+                              alpha=alpha, beta=beta, c_in=c_in)
+
+
+def grouped_gemm_dgrad_unaligned(a: dict, b_t: dict, ws: np.ndarray, G: int, N: int, K: int,
+                                 alpha=None, beta=None, c_in=None, bias=None):
+    """dgrad NN (MXFP8) for groups of any size: a = rowwise dY (dense data,
+    padded scales); b_t = colwise copy of W as in grouped_gemm_dgrad."""
+    offs, poffs = live_rows(ws, G), padded_rows(ws, G)
+    q_pad = _padded_rowwise(a, ws, G, N)
+    al = _per_group(alpha, G)
+    be = np.zeros(G) if beta is None else np.asarray(beta, np.float64).reshape(G)
+    WT = dequantize_rows("mxfp8", b_t["q"], b_t["sf"], G * N, np.arange(K))
+    rows = np.arange(offs[-1])
+    out = np.zeros((rows.size, K), np.float64)
+    for g in range(G):
+        m = int(ws[g])
+        if m == 0:
+            continue
+        A = dequantize_rows("mxfp8", q_pad, a["sf"], N, poffs[g] + np.arange(m))
+        res = al[g] * (A @ WT[:, g * N:(g + 1) * N].T)
+        if bias is not None:
+            res = res + np.asarray(bias, np.float64)[g][None, :]
+        r = offs[g] + np.arange(m)
+        if c_in is not None and be[g] != 0.0:
+            res = res + be[g] * np.asarray(c_in, np.float64)[r]
+        out[r] = res
+    return rows, out

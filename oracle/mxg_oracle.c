@@ -175,8 +175,9 @@ ORACLE_API void mxg_oracle_swizzle(const uint8_t* plain, int64_t R, int64_t C, u
 /* cut off (SUM_OVER_CAPACITY).  The workspace holds the sanitised sizes.   */
 /* Returns the status bits.                                                 */
 /* ------------------------------------------------------------------------ */
-ORACLE_API int32_t mxg_oracle_group_offsets(const int64_t* sizes, int G, int64_t multiplier,
-                                            int64_t last_dim, int64_t rows_capacity, int64_t* ws) {
+static int32_t group_offsets_rule(const int64_t* sizes, int G, int64_t multiplier,
+                                  int64_t last_dim, int64_t rows_capacity, int64_t* ws,
+                                  int round128) {
   int32_t st = 0;
   int64_t rows_before = 0;
   ws[G] = 0;
@@ -186,7 +187,7 @@ ORACLE_API int32_t mxg_oracle_group_offsets(const int64_t* sizes, int G, int64_t
       st |= ORACLE_ST_NEG_SIZE;
       s = 0;
     }
-    if (s % 128 != 0) {
+    if (round128 && s % 128 != 0) {
       st |= ORACLE_ST_MISALIGNED;
       s -= s % 128;
     }
@@ -199,6 +200,21 @@ ORACLE_API int32_t mxg_oracle_group_offsets(const int64_t* sizes, int G, int64_t
     ws[G + 1 + g] = ws[G + g] + s * last_dim;
   }
   return st;
+}
+
+/* Sizes rounded down to multiples of 128 (the aligned contract). */
+ORACLE_API int32_t mxg_oracle_group_offsets(const int64_t* sizes, int G, int64_t multiplier,
+                                            int64_t last_dim, int64_t rows_capacity, int64_t* ws) {
+  return group_offsets_rule(sizes, G, multiplier, last_dim, rows_capacity, ws, 1);
+}
+
+/* Sizes kept as given (groups of any size: [PR2763] review thread, the
+   128-row rule comes from the offset arithmetic of the quantize and GEMM
+   setup, not from the GEMM). */
+ORACLE_API int32_t mxg_oracle_group_offsets_unaligned(const int64_t* sizes, int G,
+                                                      int64_t multiplier, int64_t last_dim,
+                                                      int64_t rows_capacity, int64_t* ws) {
+  return group_offsets_rule(sizes, G, multiplier, last_dim, rows_capacity, ws, 0);
 }
 
 /* ------------------------------------------------------------------------ */
