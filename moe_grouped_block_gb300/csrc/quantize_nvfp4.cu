@@ -159,6 +159,123 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------------
+// Rows staged in shared memory.  Each warp owns one row buffer; lane 0
+// brings a whole row in with one bulk copy (completing on the buffer's
+// mbarrier), so HBM and L2 see every row once and both passes read shared
+// memory.  The block arithmetic is the one above, step for step; the row
+// amax uses the packed bf16 maximum (exact).  One buffer per warp, not two:
+// the per-block chain (two IEEE divisions, then the conversions) is latency
+// bound and wants warps more than it wants a second row in flight
+// (measured on the 16384 x 7168 activations: 0.068 ms with 16 warps of one
+// buffer per SM, 0.085 ms with 8 warps of two).  Used for cols <= 7168, where
+// two CTAs of 8 warps fit in an SM's shared memory.
+// ------------------------------------------------------------------------
+constexpr int kNvRowWarps = 8;
+constexpr int64_t kNvRowMaxCols = 7168;
+
+__device__ __forceinline__ float amax8_packed(const uint4 v) {
+  const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w));
+  return fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+}
+
+__global__ void __launch_bounds__(32 * kNvRowWarps)
+    nvfp4_quantize_rows_smem_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
+                                    const int64_t* __restrict__ group_ws, int G,
+                                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                    float* __restrict__ outer, int32_t* status) {
+  extern __shared__ __align__(128) uint8_t nsm[];
+  __shared__ uint64_t bars[kNvRowWarps];
+  __shared__ int64_t live_s;
+  __shared__ int abort_s;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint32_t row_bytes = static_cast<uint32_t>(cols * 2);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNvRowWarps; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    abort_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    const int64_t l = live_rows_warp_nv(group_ws, G, cap, status);
+    if (lane == 0) live_s = l;
+  }
+  __syncthreads();
+  const int64_t live = live_s;
+  const int64_t nb = cols >> 4;  // 16-element blocks per row
+  const int64_t C4 = nb >> 2;    // swizzle tiles per 128-row band
+  volatile int* abort_flag = &abort_s;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kNvRowWarps;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kNvRowWarps + warp;
+  uint8_t* buf = nsm + static_cast<size_t>(warp) * row_bytes;
+  const uint32_t bar = smem_u32(&bars[warp]);
+  auto issue = [&](int64_t r) {
+    mbar_arrive_expect_tx(bar, row_bytes);
+    bulk_load(smem_u32(buf), x + r * cols, row_bytes, bar);
+  };
+  if (lane == 0 && r0 < live) issue(r0);
+  uint32_t parity = 0u;
+  bool pending = r0 < live;
+  for (int64_t r = r0; r < live; r += stride) {
+    if (!mbar_wait(bar, parity, abort_flag, status)) break;
+    parity ^= 1u;
+    pending = false;
+    const uint4* row = reinterpret_cast<const uint4*>(buf);
+    // pass 1: row amax
+    float a = 0.f;
+    for (int64_t c = lane; c < (cols >> 3); c += 32) a = fmaxf(a, amax8_packed(row[c]));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
+    const bool zero_row = !(a > 0.f);
+    const float S = zero_row ? 0.f : __fdiv_rn(2688.0f, a);
+    if (lane == 0) outer[r] = zero_row ? 0.f : __fdiv_rn(a, 2688.0f);
+    // pass 2: blocks (lane = block within a run of 32)
+    const int64_t rb = (r >> 7) * C4 * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+    for (int64_t b0 = 0; b0 < nb; b0 += 32) {
+      const int64_t blk = b0 + lane;
+      const bool act = blk < nb;  // nb % 4 == 0: groups of 4 lanes agree
+      uint32_t sbyte = 0;
+      if (act) {
+        const uint4 v0 = row[2 * blk], v1 = row[2 * blk + 1];
+        uint2 o;
+        if (!zero_row) {
+          const float ab = fmaxf(amax8_packed(v0), amax8_packed(v1));
+          const float t = __fmul_rn(__fdiv_rn(ab, 6.0f), S);
+          sbyte = cvt_e4m3x2(t, 0.f) & 0x7Fu;
+        }
+        const float sbv = ue4m3_value(sbyte);
+        if (sbv == 0.f) {
+          o.x = sign_nibbles8(v0);
+          o.y = sign_nibbles8(v1);
+        } else {
+          const float ratio = __fdiv_rn(S, sbv);
+          o.x = e2m1_8(v0, ratio);
+          o.y = e2m1_8(v1, ratio);
+        }
+        *reinterpret_cast<uint2*>(q + r * (cols >> 1) + 8 * blk) = o;
+      }
+      const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 1);
+      const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 2);
+      const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sbyte, 3);
+      if (act && (lane & 3u) == 0)
+        *reinterpret_cast<uint32_t*>(sf + rb + (blk >> 2) * 512) =
+            sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+    }
+    // every lane is done with the buffer before it is refilled
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0 && r + stride < live) {
+      issue(r + stride);
+      pending = true;
+    }
+  }
+  // a copy still in flight (only after an abort) lands before the CTA exits
+  if (lane == 0 && pending) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+      if (globaltimer() - t0 > kWaitTimeoutNs) break;
+  }
+}
+
+// ------------------------------------------------------------------------
 // Colwise (transposed) row-scaled NVFP4: the copy wgrad consumes (PR #3661
 // sizes the columnwise amax per column and splits it per expert).  For group
 // g and column k the outer scale is A[g,k] / 2688 with A the column amax over
@@ -348,6 +465,24 @@ cudaError_t launch_nvfp4_quantize(const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q, uint8_t* sf,
                                   float* outer, int32_t* status, int num_sms, cudaStream_t stream) {
   if (cap == 0) return cudaSuccess;
+  if (cols <= kNvRowMaxCols) {  // one row per warp in shared memory
+    const size_t smem = static_cast<size_t>(kNvRowWarps) * static_cast<size_t>(cols) * 2;
+    auto kern = nvfp4_quantize_rows_smem_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kNvRowWarps, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    const int64_t max_ctas = (cap + kNvRowWarps - 1) / kNvRowWarps;
+    const int64_t full = static_cast<int64_t>(num_sms) * per_sm;
+    const int grid = static_cast<int>(max_ctas < full ? max_ctas : full);
+    kern<<<grid, 32 * kNvRowWarps, smem, stream>>>(x, cap, cols, group_ws, G, q, sf, outer,
+                                                   status);
+    return cudaGetLastError();
+  }
   const int64_t max_ctas = (cap + 7) / 8;
   const int grid = static_cast<int>(max_ctas < num_sms * 8 ? max_ctas : num_sms * 8);
   nvfp4_quantize_kernel<<<grid, 256, 0, stream>>>(x, cap, cols, group_ws, G, q, sf, outer, status);

@@ -156,6 +156,15 @@ def test_nvfp4_scaled_workload():
     _check_nvfp4(inp["w"].reshape(-1, wl.K)[:512], None, 1, 512)
 
 
+@pytest.mark.parametrize("cols", [7168, 7296])
+def test_nvfp4_row_width_either_side_of_staging_limit(cols):
+    # rows up to 7168 columns are staged whole in shared memory; wider rows
+    # take the kernel that reads them twice from global memory
+    R = 256
+    x = workloads.random_bf16((R, cols), seed=12, dist="uniform", scale=3.0)
+    _check_nvfp4(x, None, 1, R)
+
+
 def test_nvfp4_special_rows():
     R, C = 256, 384
     x = workloads.random_bf16((R, C), seed=9, dist="student_t3").to(torch.float32)
