@@ -617,15 +617,18 @@ struct PairCfg {
   static constexpr int kSfbBytes = 512 * kAtomsK * 2;
   static constexpr int kStageBytes =
       ((kATile + kBTile + kSfaBytes + kSfbBytes + 1023) / 1024) * 1024;
-  // bytes landing per stage in BOTH CTAs, counted on the even CTA's barrier
-  static constexpr uint32_t kTxBytes = 2u * (kATile + kBTile + kSfaBytes + kSfbBytes);
+  // bytes landing per stage in BOTH CTAs, counted on the even CTA's barriers:
+  // the operand tiles on full[s], the scale tiles on sffull[s]
+  static constexpr uint32_t kTxBytes = 2u * (kATile + kBTile);
+  static constexpr uint32_t kTxSfBytes = 2u * (kSfaBytes + kSfbBytes);
   static constexpr int kSfaCols = 4 * kAtomsK;
   static constexpr int kSfCols = kSfaCols * 3;
   static constexpr int kTmemCols = 512;
   static_assert(BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
   static constexpr int kSfCopies = 3 * kAtomsK;  // scale tiles per stage (A, then B bands)
-  // full[S], empty[S], sfready[S], tfull, tempty, drain, sfdrain; TMEM base; abort flag
-  static constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
+  // full[S], empty[S], sfready[S], sffull[S], tfull, tempty, drain, sfdrain;
+  // TMEM base; abort flag
+  static constexpr int kBarBytes = 8 * (4 * STAGES + 4) + 16;
   static size_t smem_bytes(int G) {
     return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16;
   }
@@ -707,7 +710,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * STAGES + 4));
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (4 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
@@ -719,10 +722,11 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
   auto sfready_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + s]); };
-  const uint32_t tfull_bar = smem_u32(&bars[3 * STAGES]);
-  const uint32_t tempty_bar = smem_u32(&bars[3 * STAGES + 1]);
-  const uint32_t drain_bar = smem_u32(&bars[3 * STAGES + 2]);
-  const uint32_t sfdrain_bar = smem_u32(&bars[3 * STAGES + 3]);
+  auto sffull_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + s]); };
+  const uint32_t tfull_bar = smem_u32(&bars[4 * STAGES]);
+  const uint32_t tempty_bar = smem_u32(&bars[4 * STAGES + 1]);
+  const uint32_t drain_bar = smem_u32(&bars[4 * STAGES + 2]);
+  const uint32_t sfdrain_bar = smem_u32(&bars[4 * STAGES + 3]);
   constexpr uint32_t kFirstSfWarp = 2 + Cfg::kEpiWarps;
 
   // ------------------------------------------------------------ set-up
@@ -731,6 +735,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       mbar_init(full_bar(s), 1);   // even CTA: its producer's arrival + both CTAs' bytes
       mbar_init(empty_bar(s), 1);  // the pair's MMA commit
       mbar_init(sfready_bar(s), Cfg::kSfWarps);  // even CTA: the scale-copy warps' commits
+      mbar_init(sffull_bar(s), 1);  // even CTA: its producer's arrival + both CTAs' scale bytes
     }
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 2 * Cfg::kEpiWarps);  // even CTA: both CTAs' epilogue warps
@@ -779,18 +784,24 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
           const uint32_t sb = sa + Cfg::kATile;
           const uint32_t ssfa = sb + Cfg::kBTile;
           const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), Cfg::kTxBytes);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(sffull_bar(stage), Cfg::kTxSfBytes);
+            mbar_arrive_expect_tx(full_bar(stage), Cfg::kTxBytes);
+          }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const uint32_t sfb_bar = mapa_shared(sffull_bar(stage), 0);
           const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
+          // scale tiles first, on their own barrier: this CTA's A band, both B
+          // bands of the unit.  They land well before the operand tiles, so
+          // the copy warps move them into tensor memory meanwhile.
+          const int64_t a_atom = NVF4 ? ka * Cfg::kAtomsK : ka;
+          const int64_t b_atom = NVF4 ? kbb * Cfg::kAtomsK : kbb;
+          tma_load_2d_pair(ssfa, &tmap_sfa, sfb_bar, 0,
+                           static_cast<int32_t>(a_band * p.a_atoms_row + a_atom));
+          tma_load_3d_pair(ssfb, &tmap_sfb, sfb_bar, 0, static_cast<int32_t>(b_atom), b_band);
           tma_load_2d_pair(sa, &tmap_a, fb, static_cast<int32_t>(ka * BK),
                            static_cast<int32_t>(ti.a_row));
           tma_load_2d_pair(sb, &tmap_b, fb, static_cast<int32_t>(kbb * BK), b_half);
-          // scale tiles: this CTA's A band, both B bands of the unit
-          const int64_t a_atom = NVF4 ? ka * Cfg::kAtomsK : ka;
-          const int64_t b_atom = NVF4 ? kbb * Cfg::kAtomsK : kbb;
-          tma_load_2d_pair(ssfa, &tmap_sfa, fb, 0,
-                           static_cast<int32_t>(a_band * p.a_atoms_row + a_atom));
-          tma_load_3d_pair(ssfb, &tmap_sfb, fb, 0, static_cast<int32_t>(b_atom), b_band);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -799,12 +810,14 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
           }
         }
       }
-      // the even CTA's full barriers count both CTAs' bytes: once they have
-      // completed, every copy of the pair has landed
+      // the even CTA's full and scale barriers count both CTAs' bytes: once
+      // they have completed, every copy of the pair has landed
       if (rank == 0)
         for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s))
+          if (issued_mask & (1u << s)) {
             mbar_wait_drain(full_bar(s), (last_parity >> s) & 1u, p.status, p.timeout_ns);
+            mbar_wait_drain(sffull_bar(s), (last_parity >> s) & 1u, p.status, p.timeout_ns);
+          }
     }
   }
   // ------------------------------------------------------------ MMA issuer (even CTA)
@@ -871,8 +884,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
         bool ok = true;
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           // the stage's previous MMAs finished before its producer refilled it
-          // (empty barrier), so its scale columns are free once it is full
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+          // (empty barrier), so its scale columns are free once its scale
+          // tiles have landed
+          if (!mbar_wait(sffull_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
