@@ -159,18 +159,20 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------------
-// Rows staged in shared memory.  Each warp owns one row buffer; lane 0
-// brings a whole row in with one bulk copy (completing on the buffer's
-// mbarrier), so HBM and L2 see every row once and both passes read shared
-// memory.  The block arithmetic is the one above, step for step; the row
-// amax uses the packed bf16 maximum (exact).  One buffer per warp, not two:
-// the per-block chain (two IEEE divisions, then the conversions) is latency
-// bound and wants warps more than it wants a second row in flight
-// (measured on the 16384 x 7168 activations: 0.068 ms with 16 warps of one
-// buffer per SM, 0.085 ms with 8 warps of two).  Used for cols <= 7168, where
-// two CTAs of 8 warps fit in an SM's shared memory.
+// Rows staged in shared memory.  A pair of warps owns one row buffer; one
+// lane brings a whole row in with a single bulk copy (completing on the
+// buffer's mbarrier), so HBM and L2 see every row once and both passes read
+// shared memory.  Each warp of the pair reduces half of the row for the row
+// amax (combined through shared memory at a pair barrier) and quantizes half
+// of its blocks.  The block arithmetic is the one above, step for step; the
+// row amax uses the packed bf16 maximum (exact).  The per-block chain (two
+// IEEE divisions, then the conversions) is latency bound, so what counts is
+// warps per SM: two warps per staged row give 32 warps on the 16 rows that
+// fit (measured on the 16384 x 7168 activations: 0.085 ms with 8 warps of
+// two buffers each, 0.068 ms with 16 warps of one).  Used for cols <= 7168,
+// where two CTAs of 8 rows fit in an SM's shared memory.
 // ------------------------------------------------------------------------
-constexpr int kNvRowWarps = 8;
+constexpr int kNvRowPairs = 8;  // rows in flight per CTA, two warps each
 constexpr int64_t kNvRowMaxCols = 7168;
 
 __device__ __forceinline__ float amax8_packed(const uint4 v) {
@@ -178,19 +180,41 @@ __device__ __forceinline__ float amax8_packed(const uint4 v) {
   return fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
 }
 
-__global__ void __launch_bounds__(32 * kNvRowWarps)
+// Barrier over the 64 threads of warp pair `pair` (named barrier pair + 1).
+__device__ __forceinline__ void pair_sync(uint32_t pair) {
+  asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
+}
+
+// Same, returning whether `ok` holds in every thread of the pair.
+__device__ __forceinline__ bool pair_all(uint32_t pair, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %2, 0;\n\t"
+      "bar.red.and.pred q, %1, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pair + 1), "r"(ok ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(64 * kNvRowPairs, 2)
     nvfp4_quantize_rows_smem_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
                                     const int64_t* __restrict__ group_ws, int G,
                                     uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                     float* __restrict__ outer, int32_t* status) {
   extern __shared__ __align__(128) uint8_t nsm[];
-  __shared__ uint64_t bars[kNvRowWarps];
+  __shared__ uint64_t bars[kNvRowPairs];
+  __shared__ float part[kNvRowPairs][2];
   __shared__ int64_t live_s;
   __shared__ int abort_s;
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  const uint32_t pair = warp >> 1, half = warp & 1u;
+  const bool leader = half == 0 && lane == 0;
   const uint32_t row_bytes = static_cast<uint32_t>(cols * 2);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNvRowWarps; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    for (int i = 0; i < kNvRowPairs; ++i) mbar_init(smem_u32(&bars[i]), 1);
     abort_s = 0;
     fence_barrier_init();
   }
@@ -200,38 +224,46 @@ __global__ void __launch_bounds__(32 * kNvRowWarps)
   }
   __syncthreads();
   const int64_t live = live_s;
-  const int64_t nb = cols >> 4;  // 16-element blocks per row
-  const int64_t C4 = nb >> 2;    // swizzle tiles per 128-row band
+  const int64_t nb = cols >> 4;   // 16-element blocks per row (a multiple of 8)
+  const int64_t C4 = nb >> 2;     // swizzle tiles per 128-row band
+  const int64_t hb = nb >> 1;     // blocks per warp of the pair (a multiple of 4)
+  const int64_t hc = cols >> 4;   // 16-byte chunks per warp of the pair (cols / 8 / 2)
   volatile int* abort_flag = &abort_s;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kNvRowWarps;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kNvRowWarps + warp;
-  uint8_t* buf = nsm + static_cast<size_t>(warp) * row_bytes;
-  const uint32_t bar = smem_u32(&bars[warp]);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kNvRowPairs;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kNvRowPairs + pair;
+  uint8_t* buf = nsm + static_cast<size_t>(pair) * row_bytes;
+  const uint32_t bar = smem_u32(&bars[pair]);
   auto issue = [&](int64_t r) {
     mbar_arrive_expect_tx(bar, row_bytes);
     bulk_load(smem_u32(buf), x + r * cols, row_bytes, bar);
   };
-  if (lane == 0 && r0 < live) issue(r0);
+  if (leader && r0 < live) issue(r0);
   uint32_t parity = 0u;
   bool pending = r0 < live;
   for (int64_t r = r0; r < live; r += stride) {
-    if (!mbar_wait(bar, parity, abort_flag, status)) break;
+    // both warps of the pair take the same decision, so neither is left at a
+    // pair barrier the other never reaches
+    if (!pair_all(pair, mbar_wait(bar, parity, abort_flag, status))) break;
     parity ^= 1u;
     pending = false;
     const uint4* row = reinterpret_cast<const uint4*>(buf);
-    // pass 1: row amax
+    // pass 1: row amax (this warp's half of the chunks, then the pair's)
     float a = 0.f;
-    for (int64_t c = lane; c < (cols >> 3); c += 32) a = fmaxf(a, amax8_packed(row[c]));
+    for (int64_t c = half * hc + lane; c < (half + 1) * hc; c += 32) a = fmaxf(a, amax8_packed(row[c]));
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
+    if (lane == 0) part[pair][half] = a;
+    pair_sync(pair);
+    a = fmaxf(part[pair][0], part[pair][1]);
     const bool zero_row = !(a > 0.f);
     const float S = zero_row ? 0.f : __fdiv_rn(2688.0f, a);
-    if (lane == 0) outer[r] = zero_row ? 0.f : __fdiv_rn(a, 2688.0f);
-    // pass 2: blocks (lane = block within a run of 32)
+    if (leader) outer[r] = zero_row ? 0.f : __fdiv_rn(a, 2688.0f);
+    // pass 2: this warp's half of the blocks (lane = block within a run of 32)
     const int64_t rb = (r >> 7) * C4 * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4;
-    for (int64_t b0 = 0; b0 < nb; b0 += 32) {
+    const int64_t bend = (half + 1) * hb;
+    for (int64_t b0 = half * hb; b0 < bend; b0 += 32) {
       const int64_t blk = b0 + lane;
-      const bool act = blk < nb;  // nb % 4 == 0: groups of 4 lanes agree
+      const bool act = blk < bend;  // hb % 4 == 0: groups of 4 lanes agree
       uint32_t sbyte = 0;
       if (act) {
         const uint4 v0 = row[2 * blk], v1 = row[2 * blk + 1];
@@ -259,16 +291,16 @@ __global__ void __launch_bounds__(32 * kNvRowWarps)
         *reinterpret_cast<uint32_t*>(sf + rb + (blk >> 2) * 512) =
             sbyte | (s1 << 8) | (s2 << 16) | (s3 << 24);
     }
-    // every lane is done with the buffer before it is refilled
+    // both warps are done with the buffer (and part[]) before it is refilled
     fence_proxy_async_shared();
-    __syncwarp();
-    if (lane == 0 && r + stride < live) {
+    pair_sync(pair);
+    if (leader && r + stride < live) {
       issue(r + stride);
       pending = true;
     }
   }
   // a copy still in flight (only after an abort) lands before the CTA exits
-  if (lane == 0 && pending) {
+  if (leader && pending) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
       if (globaltimer() - t0 > kWaitTimeoutNs) break;
@@ -465,21 +497,21 @@ cudaError_t launch_nvfp4_quantize(const uint16_t* x, int64_t cap, int64_t cols,
                                   const int64_t* group_ws, int G, uint8_t* q, uint8_t* sf,
                                   float* outer, int32_t* status, int num_sms, cudaStream_t stream) {
   if (cap == 0) return cudaSuccess;
-  if (cols <= kNvRowMaxCols) {  // one row per warp in shared memory
-    const size_t smem = static_cast<size_t>(kNvRowWarps) * static_cast<size_t>(cols) * 2;
+  if (cols <= kNvRowMaxCols) {  // one row per warp pair in shared memory
+    const size_t smem = static_cast<size_t>(kNvRowPairs) * static_cast<size_t>(cols) * 2;
     auto kern = nvfp4_quantize_rows_smem_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kNvRowWarps, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 64 * kNvRowPairs, smem) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
-    const int64_t max_ctas = (cap + kNvRowWarps - 1) / kNvRowWarps;
+    const int64_t max_ctas = (cap + kNvRowPairs - 1) / kNvRowPairs;
     const int64_t full = static_cast<int64_t>(num_sms) * per_sm;
     const int grid = static_cast<int>(max_ctas < full ? max_ctas : full);
-    kern<<<grid, 32 * kNvRowWarps, smem, stream>>>(x, cap, cols, group_ws, G, q, sf, outer,
+    kern<<<grid, 64 * kNvRowPairs, smem, stream>>>(x, cap, cols, group_ws, G, q, sf, outer,
                                                    status);
     return cudaGetLastError();
   }
