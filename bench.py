@@ -176,7 +176,7 @@ class ClockSampler:
 class Path:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, wl, out_bf16: bool, dev, rank: int = 0):
+    def __init__(self, wl, out_bf16: bool, dev, rank: int = 0, epilogue: str = "none"):
         import torch
         from moe_grouped_block_gb300 import mxg, workloads
         self.mxg, self.torch = mxg, torch
@@ -186,25 +186,46 @@ class Path:
         self.host = inp
         G, N, K, R = wl.G, wl.N, wl.K, wl.rows_capacity
         self.G, self.N, self.K, self.R = G, N, K, R
+        self.unaligned = wl.sizes == "dirichlet_rows"
         self.sizes = inp["sizes"].to(dev)
-        self.x = inp["x"].to(dev)
         self.ws = mxg.alloc_offsets(G, dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out_type = mxg.MXG_OUT_BF16 if out_bf16 else mxg.MXG_OUT_F32
         cdt = torch.bfloat16 if out_bf16 else torch.float32
+        # per-group bias and alpha in the GEMM epilogue (fprop only)
+        self.bias = self.alpha = None
+        if epilogue == "bias_alpha":
+            g = torch.Generator().manual_seed(wl.seed)
+            self.bias = torch.randn((G, N), generator=g).float().to(dev)
+            self.alpha = (0.5 + torch.rand(G, generator=g)).float().to(dev)
         if wl.mode == "fprop":
+            self.x = inp["x"].to(dev)
             self.w = inp["w"].to(dev).reshape(G * N, K)
-            if wl.fmt == "mxfp8":
+            if self.unaligned:
+                self.qx = mxg.alloc_mxfp8_unaligned(R, K, G, rowwise=True, colwise=True, device=dev)
+                self.qw = mxg.alloc_mxfp8(G * N, K, device=dev)
+            elif wl.fmt == "mxfp8":
                 self.qx = mxg.alloc_mxfp8(R, K, rowwise=True, colwise=True, device=dev)
                 self.qw = mxg.alloc_mxfp8(G * N, K, device=dev)
             else:
                 self.qx = mxg.alloc_nvfp4(R, K, device=dev)
                 self.qw = mxg.alloc_nvfp4(G * N, K, device=dev)
             self.C = torch.empty((R, N), dtype=cdt, device=dev)
-        else:
+        elif wl.mode == "dgrad":
             self.dy = inp["dy"].to(dev)
-            self.qx = mxg.alloc_mxfp8(R, K, rowwise=False, colwise=True, device=dev)
-            self.qd = mxg.alloc_mxfp8(R, N, rowwise=False, colwise=True, device=dev)
+            self.w = inp["w"].to(dev).reshape(G * N, K)
+            self.qd = mxg.alloc_mxfp8(R, N, device=dev)
+            self.qwt = mxg.alloc_mxfp8(G * N, K, rowwise=False, colwise=True, device=dev)
+            self.C = torch.empty((R, K), dtype=cdt, device=dev)
+        else:
+            self.x = inp["x"].to(dev)
+            self.dy = inp["dy"].to(dev)
+            if wl.fmt == "mxfp8":
+                self.qx = mxg.alloc_mxfp8(R, K, rowwise=False, colwise=True, device=dev)
+                self.qd = mxg.alloc_mxfp8(R, N, rowwise=False, colwise=True, device=dev)
+            else:
+                self.qx = mxg.alloc_nvfp4(R, K, device=dev, rowwise=False, colwise=True, G=G)
+                self.qd = mxg.alloc_nvfp4(R, N, device=dev, rowwise=False, colwise=True, G=G)
             self.C = torch.empty((G, N, K), dtype=cdt, device=dev)
 
     # each stage returns nothing; all work is enqueued on the current stream
@@ -212,9 +233,48 @@ class Path:
         m, wl = self.mxg, self.wl
         G, N, K, R = self.G, self.N, self.K, self.R
         out = []
-        out.append(("group_offsets", lambda: m.mxg_group_offsets(self.sizes, 1, K, R, self.ws,
-                                                                 self.status)))
-        if wl.mode == "fprop" and wl.fmt == "mxfp8":
+        if self.unaligned:
+            out.append(("group_offsets", lambda: m.mxg_group_offsets_unaligned(
+                self.sizes, 1, K, R, self.ws, self.status)))
+        else:
+            out.append(("group_offsets", lambda: m.mxg_group_offsets(
+                self.sizes, 1, N if wl.mode == "dgrad" else K, R, self.ws, self.status)))
+        if self.unaligned:
+            q = self.qx
+            out.append(("quantize_x_mxfp8_both", lambda: m.mxg_group_quantize_unaligned(
+                m.MXG_BOTH, self.x, R, K, self.ws, G, q["q_row"], q["sf_row"], q["q_col"],
+                q["sf_col"], self.status)))
+            out.append(("quantize_w_mxfp8_row", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_ROWWISE, self.w, G * N, K, None, G, self.qw["q_row"],
+                self.qw["sf_row"], None, None, None, self.status)))
+            out.append(("grouped_gemm_fprop_mxfp8", lambda: m.mxg_grouped_gemm_unaligned(
+                m.MXG_FPROP_TN, (q["q_row"], q["sf_row"]), (self.qw["q_row"], self.qw["sf_row"]),
+                self.ws, G, R, N, K, alpha=self.alpha, C=self.C, out_type=self.out_type,
+                dev_status=self.status, bias=self.bias)))
+        elif wl.mode == "dgrad":
+            out.append(("quantize_dy_mxfp8_row", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_ROWWISE, self.dy, R, N, self.ws, G, self.qd["q_row"],
+                self.qd["sf_row"], None, None, None, self.status)))
+            out.append(("quantize_w_mxfp8_col", lambda: m.mxg_group_quantize(
+                m.MXG_MXFP8_E4M3, m.MXG_COLWISE, self.w, G * N, K, None, G, None, None,
+                self.qwt["q_col"], self.qwt["sf_col"], None, self.status)))
+            out.append(("grouped_gemm_dgrad_mxfp8", lambda: m.mxg_grouped_gemm(
+                m.MXG_MXFP8_E4M3, m.MXG_DGRAD_NN, (self.qd["q_row"], self.qd["sf_row"], None),
+                (self.qwt["q_col"], self.qwt["sf_col"], None), self.ws, G, R, N, K, C=self.C,
+                out_type=self.out_type, dev_status=self.status)))
+        elif wl.mode == "wgrad" and wl.fmt == "nvfp4":
+            qx, qd = self.qx, self.qd
+            out.append(("quantize_x_nvfp4_col", lambda: m.mxg_group_quantize(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_COLWISE, self.x, R, K, self.ws, G, None, None,
+                qx["q_col"], qx["sf_col"], None, self.status, outer_col=qx["outer_col"])))
+            out.append(("quantize_dy_nvfp4_col", lambda: m.mxg_group_quantize(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_COLWISE, self.dy, R, N, self.ws, G, None, None,
+                qd["q_col"], qd["sf_col"], None, self.status, outer_col=qd["outer_col"])))
+            out.append(("grouped_gemm_wgrad_nvfp4", lambda: m.mxg_grouped_gemm(
+                m.MXG_NVFP4_ROWSCALED, m.MXG_WGRAD_NT, (qd["q_col"], qd["sf_col"], qd["outer_col"]),
+                (qx["q_col"], qx["sf_col"], qx["outer_col"]), self.ws, G, R, N, K, C=self.C,
+                out_type=self.out_type, dev_status=self.status)))
+        elif wl.mode == "fprop" and wl.fmt == "mxfp8":
             q = self.qx
             out.append(("quantize_x_mxfp8_both", lambda: m.mxg_group_quantize(
                 m.MXG_MXFP8_E4M3, m.MXG_BOTH, self.x, R, K, self.ws, G, q["q_row"], q["sf_row"],
@@ -224,8 +284,9 @@ class Path:
                 self.qw["sf_row"], None, None, None, self.status)))
             out.append(("grouped_gemm_fprop_mxfp8", lambda: m.mxg_grouped_gemm(
                 m.MXG_MXFP8_E4M3, m.MXG_FPROP_TN, (q["q_row"], q["sf_row"], None),
-                (self.qw["q_row"], self.qw["sf_row"], None), self.ws, G, R, N, K, C=self.C,
-                out_type=self.out_type, dev_status=self.status)))
+                (self.qw["q_row"], self.qw["sf_row"], None), self.ws, G, R, N, K,
+                alpha=self.alpha, C=self.C, out_type=self.out_type, dev_status=self.status,
+                bias=self.bias)))
         elif wl.mode == "fprop":
             q, qw = self.qx, self.qw
             out.append(("quantize_x_nvfp4", lambda: m.mxg_group_quantize(
@@ -271,10 +332,24 @@ class Path:
             return M * K * (2 + 1 + 1 / 32)
         if name == "quantize_dy_mxfp8_col":
             return M * N * (2 + 1 + 1 / 32)
+        if name == "quantize_dy_mxfp8_row":
+            return M * N * (2 + 1 + 1 / 32)
+        if name == "quantize_w_mxfp8_col":
+            return G * N * K * (2 + 1 + 1 / 32)
+        if name == "quantize_x_nvfp4_col":  # + the [G, K] outer scales
+            return M * K * (2 + 0.5 + 1 / 16) + 4 * G * K
+        if name == "quantize_dy_nvfp4_col":
+            return M * N * (2 + 0.5 + 1 / 16) + 4 * G * N
         sizes = self.host["sizes"].numpy()
         live_experts = int((sizes > 0).sum())
+        extra = 0 if self.bias is None else 4 * G * (N + 1)
         if name == "grouped_gemm_fprop_mxfp8":
-            return M * K * (1 + 1 / 32) + live_experts * N * K * (1 + 1 / 32) + M * N * obytes
+            return (M * K * (1 + 1 / 32) + live_experts * N * K * (1 + 1 / 32) + M * N * obytes
+                    + extra)
+        if name == "grouped_gemm_dgrad_mxfp8":
+            return M * N * (1 + 1 / 32) + live_experts * N * K * (1 + 1 / 32) + M * K * obytes
+        if name == "grouped_gemm_wgrad_nvfp4":
+            return (N + K) * M * (0.5 + 1 / 16) + 4 * G * (N + K) + G * N * K * obytes
         if name == "grouped_gemm_fprop_nvfp4":
             return (M * K * (0.5 + 1 / 16) + live_experts * N * K * (0.5 + 1 / 16) + M * N * obytes
                     + 4 * (M + live_experts * N))
@@ -285,6 +360,8 @@ class Path:
     def input_tensors(self):
         if self.wl.mode == "fprop":
             return [("sizes", self.sizes), ("x", self.x), ("w", self.w)]
+        if self.wl.mode == "dgrad":
+            return [("sizes", self.sizes), ("dy", self.dy), ("w", self.w)]
         return [("sizes", self.sizes), ("x", self.x), ("dy", self.dy)]
 
 
@@ -331,7 +408,7 @@ def run_mxg(args, wl, ws_world, rank, local):
     if ws_world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    path = Path(wl, args.out == "bf16", dev, rank=rank)
+    path = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue)
     stages = path.stages()
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -420,7 +497,7 @@ def run_mxg(args, wl, ws_world, rank, local):
         "dtype": "nvfp4(e2m1/ue4m3)->f32" if nvfp4 else "mxfp8(e4m3/e8m0)->f32",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {"workload": wl.name, "G": wl.G, "K": wl.K, "N": wl.N, "M": wl.M,
-                   "mode": wl.mode, "out": args.out,
+                   "mode": wl.mode, "out": args.out, "epilogue": args.epilogue,
                    "step": " -> ".join(n for n, _ in stages),
                    "l2": "flushed before every timed step (512 MB write); inputs also exceed L2",
                    "parallelism": "replicas" if ws_world > 1 else "single GPU"},
@@ -455,7 +532,8 @@ def _oracle_sample(wl, rows_per_group: int, cols_per_group: int):
     G, N, K = wl.G, wl.N, wl.K
     flop = 0.0
     t0 = time.perf_counter()
-    ws, _ = oracle.group_offsets(sizes, 1, K, wl.rows_capacity)
+    ws, _ = (oracle.group_offsets_unaligned if wl.sizes == "dirichlet_rows" else
+             oracle.group_offsets)(sizes, 1, K, wl.rows_capacity)
     offs = oracle.live_rows(ws, G)
     for g in range(G):
         lo, hi = int(offs[g]), int(offs[g + 1])
@@ -480,15 +558,31 @@ def _oracle_sample(wl, rows_per_group: int, cols_per_group: int):
                 b = {"q": qb["q_row"], "sf": qb["sf_row"], "outer": qb["outer_row"]}
             oracle.grouped_gemm_fprop(wl.fmt, a, b, [0, r128], c128, K)
             flop += 2.0 * r128 * c128 * K
+        elif wl.mode == "dgrad":
+            ds = inp["dy"][lo2:lo2 + r128]
+            wsub = inp["w"][g, :, :c128].contiguous()  # [N, c128]: the sample's K columns
+            qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=True)
+            qwt = oracle.mxfp8_quantize(wsub, N, N, rowwise=False, colwise=True)
+            oracle.grouped_gemm_dgrad({"q": qd["q_row"], "sf": qd["sf_row"]},
+                                      {"q": qwt["q_col"], "sf": qwt["sf_col"]}, [0, r128], 1,
+                                      N, c128)
+            flop += 2.0 * r128 * N * c128
         else:
             xs = inp["x"][lo2:lo2 + r128]
             ds = inp["dy"][lo2:lo2 + r128, :c128].contiguous()
-            qx = oracle.mxfp8_quantize(xs, r128, r128, rowwise=False, colwise=True)
-            qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=False, colwise=True)
             kk = min(K, c128)
-            oracle.grouped_gemm_wgrad({"q": qd["q_col"], "sf": qd["sf_col"]},
-                                      {"q": qx["q_col"], "sf": qx["sf_col"]}, [0, r128], r128,
-                                      c128, K, sample_k=np.arange(kk))
+            if wl.fmt == "mxfp8":
+                qx = oracle.mxfp8_quantize(xs, r128, r128, rowwise=False, colwise=True)
+                qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=False, colwise=True)
+                a = {"q": qd["q_col"], "sf": qd["sf_col"]}
+                b = {"q": qx["q_col"], "sf": qx["sf_col"]}
+            else:
+                qx = oracle.nvfp4_quantize_colwise(xs, [0, r128], r128)
+                qd = oracle.nvfp4_quantize_colwise(ds, [0, r128], r128)
+                a = {"q": qd["q_col"], "sf": qd["sf_col"], "outer": qd["outer_col"]}
+                b = {"q": qx["q_col"], "sf": qx["sf_col"], "outer": qx["outer_col"]}
+            oracle.grouped_gemm_wgrad(a, b, [0, r128], r128, c128, K, sample_k=np.arange(kk),
+                                      fmt=wl.fmt)
             flop += 2.0 * r128 * c128 * kk
     return time.perf_counter() - t0, flop
 
@@ -553,6 +647,8 @@ def main():
     ap.add_argument("--impl", default="mxg", choices=["mxg", "reference"])
     ap.add_argument("--config", default="mixtral_fprop_mxfp8")
     ap.add_argument("--out", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--epilogue", default="none", choices=["none", "bias_alpha"],
+                    help="fprop: per-group bias and alpha in the GEMM epilogue")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")

@@ -19,11 +19,17 @@ finegrained_fprop_mxfp8      64  2048  1408   32768  Zipf(1.2), >= 1 empty group
                                                      0.1% of X scaled x100
 wgrad_mxfp8                  8   4096  14336  16384  Dirichlet(1); dY ~ N(0, 1e-3)
 rowscaled_fprop_nvfp4        32  7168  2048   16384  Dirichlet(1); X Student-t(3)
+wgrad_nvfp4                  8   4096  14336  16384  Dirichlet(1); row-scaled NVFP4
+dgrad_mxfp8                  8   4096  14336  16384  Dirichlet(1); dX = dY W_g
+mixtral_fprop_mxfp8_unal.    8   4096  14336  16384  Dirichlet(1) over rows: sizes
+                                                     of any value (not x128)
 ==========================  ===  ====  =====  =====  ===========================
 
 Group sizes are ``128 * Multinomial(M / 128, p)``: they sum to M exactly and
 are multiples of 128, as the 128-row alignment of the grouped quantize and
-grouped GEMM requires.  X ~ N(0, 1) and W ~ N(0, 0.02) unless stated.
+grouped GEMM requires -- except ``dirichlet_rows``, ``Multinomial(M, p)``, for
+the entry points that take groups of any size.  X ~ N(0, 1), W ~ N(0, 0.02)
+and dY ~ N(0, 1e-3) unless stated.
 """
 from __future__ import annotations
 
@@ -36,14 +42,14 @@ import numpy as np
 @dataclass(frozen=True)
 class Workload:
     name: str
-    mode: str          # "fprop" (ragged rows) or "wgrad" (ragged contraction)
+    mode: str          # "fprop", "dgrad" (ragged rows) or "wgrad" (ragged contraction)
     fmt: str           # "mxfp8" or "nvfp4"
     G: int
     K: int
     N: int
     M: int             # live rows (sum of group sizes)
     seed: int
-    sizes: str         # "fixed" | "dirichlet" | "zipf"
+    sizes: str         # "fixed" | "dirichlet" | "zipf" | "dirichlet_rows"
     fixed_sizes: tuple = ()
     x_dist: str = "normal"       # "normal" | "normal_outliers" | "student_t3"
     dy_std: float = 1e-3
@@ -72,6 +78,12 @@ WORKLOADS = {
                             "dirichlet"),
     "rowscaled_fprop_nvfp4": Workload("rowscaled_fprop_nvfp4", "fprop", "nvfp4", 32, 7168, 2048,
                                       16384, 4, "dirichlet", x_dist="student_t3"),
+    "wgrad_nvfp4": Workload("wgrad_nvfp4", "wgrad", "nvfp4", 8, 4096, 14336, 16384, 5,
+                            "dirichlet"),
+    "dgrad_mxfp8": Workload("dgrad_mxfp8", "dgrad", "mxfp8", 8, 4096, 14336, 16384, 6,
+                            "dirichlet"),
+    "mixtral_fprop_mxfp8_unaligned": Workload("mixtral_fprop_mxfp8_unaligned", "fprop", "mxfp8",
+                                              8, 4096, 14336, 16384, 7, "dirichlet_rows"),
 }
 
 
@@ -80,12 +92,15 @@ def _rng(seed: int, stream: int) -> np.random.Generator:
 
 
 def group_sizes(w: Workload) -> np.ndarray:
-    """int32 [G] row counts, multiples of 128, summing to w.M."""
+    """int32 [G] row counts summing to w.M: multiples of 128, or of any value
+    for ``dirichlet_rows``."""
     if w.sizes == "fixed":
         s = np.asarray(w.fixed_sizes, np.int64)
         assert s.size == w.G and s.sum() == w.M
         return s.astype(np.int32)
     rng = _rng(w.seed, 0)
+    if w.sizes == "dirichlet_rows":
+        return rng.multinomial(w.M, rng.dirichlet(np.ones(w.G))).astype(np.int32)
     units = w.M // 128
     if w.sizes == "dirichlet":
         p = rng.dirichlet(np.ones(w.G))
@@ -124,6 +139,7 @@ def make_inputs(w: Workload) -> dict:
 
     fprop: ``x`` bf16 [M_cap, K], ``w`` bf16 [G, N, K], ``sizes`` int32 [G].
     wgrad: ``x`` bf16 [M_cap, K], ``dy`` bf16 [M_cap, N], ``sizes`` int32 [G].
+    dgrad: ``dy`` bf16 [M_cap, N], ``w`` bf16 [G, N, K], ``sizes`` int32 [G].
     Rows >= M of ``x`` / ``dy`` are filled with draws as well (they are never
     read by the path; tests use them to check that).
     """
@@ -131,11 +147,12 @@ def make_inputs(w: Workload) -> dict:
     sizes = group_sizes(w)
     R = w.rows_capacity
     out = {"sizes": torch.from_numpy(sizes.copy())}
-    out["x"] = _bf16(_activations(w, _rng(w.seed, 1), R, w.K))
-    if w.mode == "fprop":
+    if w.mode != "dgrad":
+        out["x"] = _bf16(_activations(w, _rng(w.seed, 1), R, w.K))
+    if w.mode in ("fprop", "dgrad"):
         wr = _rng(w.seed, 2)
         out["w"] = _bf16(wr.standard_normal((w.G, w.N, w.K), dtype=np.float32) * w.w_std)
-    else:
+    if w.mode in ("wgrad", "dgrad"):
         dr = _rng(w.seed, 3)
         out["dy"] = _bf16(dr.standard_normal((R, w.N), dtype=np.float32) * w.dy_std)
     return out

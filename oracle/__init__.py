@@ -500,29 +500,33 @@ def _padded_rowwise(a: dict, ws: np.ndarray, G: int, cols: int) -> np.ndarray:
 
 
 def grouped_gemm_fprop_unaligned(a: dict, b: dict, ws: np.ndarray, G: int, N: int, K: int,
-                                 alpha=None, beta=None, c_in=None, bias=None):
+                                 alpha=None, beta=None, c_in=None, bias=None, sample_rows=None,
+                                 sample_cols=None):
     """fprop TN (MXFP8) for groups of any size: a = {"q": dense rowwise data
-    [M_cap, K], "sf": padded swizzled scales}.  Returns (rows, [rows, N])
-    over the live data rows; the per-group product is as in grouped_gemm_fprop."""
+    [M_cap, K], "sf": padded swizzled scales}.  Returns (rows, [rows, cols])
+    over the live data rows in ``sample_rows`` (default all) and the columns
+    in ``sample_cols`` (default all N); the per-group product is as in
+    grouped_gemm_fprop."""
     offs, poffs = live_rows(ws, G), padded_rows(ws, G)
     q_pad = _padded_rowwise(a, ws, G, K)
     al = _per_group(alpha, G)
     be = np.zeros(G) if beta is None else np.asarray(beta, np.float64).reshape(G)
-    rows = np.arange(offs[-1])
-    out = np.zeros((rows.size, N), np.float64)
+    rows = np.arange(offs[-1]) if sample_rows is None else np.asarray(sample_rows, np.int64)
+    cols = np.arange(N) if sample_cols is None else np.asarray(sample_cols, np.int64)
+    out = np.zeros((rows.size, cols.size), np.float64)
     for g in range(G):
-        m = int(ws[g])
-        if m == 0:
+        sel = np.nonzero((rows >= offs[g]) & (rows < offs[g + 1]))[0]
+        if sel.size == 0:
             continue
-        A = dequantize_rows("mxfp8", q_pad, a["sf"], K, poffs[g] + np.arange(m))
-        B = dequantize_rows("mxfp8", b["q"], b["sf"], K, g * N + np.arange(N))
+        r = rows[sel]
+        A = dequantize_rows("mxfp8", q_pad, a["sf"], K, poffs[g] + (r - offs[g]))
+        B = dequantize_rows("mxfp8", b["q"], b["sf"], K, g * N + cols)
         res = al[g] * (A @ B.T)
         if bias is not None:
-            res = res + np.asarray(bias, np.float64)[g][None, :]
-        r = offs[g] + np.arange(m)
+            res = res + np.asarray(bias, np.float64)[g][cols][None, :]
         if c_in is not None and be[g] != 0.0:
-            res = res + be[g] * np.asarray(c_in, np.float64)[r]
-        out[r] = res
+            res = res + be[g] * np.asarray(c_in, np.float64)[np.ix_(r, cols)]
+        out[sel] = res
     return rows, out
 
 
