@@ -600,9 +600,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
 // in its own tensor memory.  Per SM and pipeline stage that is 32 KB of
 // operands for a 128 x 256 x 128 MMA step, against 48 KB for the single-CTA
 // 128 x 256 tile, and half the MMA instructions.
-template <int STAGES, bool NVF4>
+// BKB: bytes of K per stage.  128 (128-byte swizzle) in general; 64 (64-byte
+// swizzle) for row-scaled NVFP4 where a 256-element K block does not fit:
+// wgrad over 128-row groups (64 bytes of E2M1 along the contraction) and fprop
+// with K % 256 != 0.
+template <int STAGES, bool NVF4, int BKB = 128>
 struct PairCfg {
-  static constexpr int BN = 256, BK = 128;
+  static constexpr int BN = 256, BK = BKB;
+  static_assert(BK == 128 || (BK == 64 && NVF4), "64-byte stages are for NVFP4 only");
+  static constexpr int kSwizzle = BK == 128 ? 2 : 4;  // descriptor swizzle mode
   static constexpr int kEpiWarps = 8;
   // scale-copy warps (even CTA): each tcgen05 instruction costs the issuing
   // thread about as long as a quarter of a stage's MMA work, so the scale
@@ -649,11 +655,10 @@ struct PairCfg {
 // on the padded offsets, so unaligned groups (a last 128-row tile partly past
 // the group) need nothing else: A's data rows start at the group's row
 // offset, its scale rows (a_sf_row) and its colwise slabs at the padded one.
-template <int EPB>
+template <int EPB, int BK>
 __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p,
                                                   const int32_t* row_off, const int32_t* prow_off,
                                                   const int32_t* tile_off, uint32_t rank) {
-  constexpr int BK = 128;
   TileInfo ti;
   ti.dup = false;
   if (p.mode != 1) {
@@ -697,13 +702,13 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
   return ti;
 }
 
-template <int STAGES, bool NVF4>
-__global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
+template <int STAGES, bool NVF4, int BKB>
+__global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b,
                              const __grid_constant__ CUtensorMap tmap_sfa,
                              const __grid_constant__ CUtensorMap tmap_sfb, const GemmParams p) {
-  using Cfg = PairCfg<STAGES, NVF4>;
+  using Cfg = PairCfg<STAGES, NVF4, BKB>;
   constexpr int BK = Cfg::BK, EPB = NVF4 ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, rank);
+        const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
         const int32_t b_half = static_cast<int32_t>(ti.b_row + 128 * rank);
         const int32_t a_band = static_cast<int32_t>(ti.a_sf_row >> 7);
         const int32_t b_band = static_cast<int32_t>(ti.b_row >> 7);
@@ -826,7 +831,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, 0);
+        const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, 0);
         if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
@@ -841,8 +846,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
           const uint32_t sb = sa + Cfg::kATile;
           const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-          const uint64_t adesc0 = smem_desc(sa, 16, 8 * BK, 2);
-          const uint64_t bdesc0 = smem_desc(sb, 16, 8 * BK, 2);
+          const uint64_t adesc0 = smem_desc(sa, 16, 8 * BK, Cfg::kSwizzle);
+          const uint64_t bdesc0 = smem_desc(sb, 16, 8 * BK, Cfg::kSwizzle);
 #pragma unroll
           for (int kk = 0; kk < Cfg::kMmas; ++kk) {
             // K step kk starts 32 bytes further along the row (16-byte units)
@@ -880,7 +885,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
       const int j = static_cast<int>(warp - kFirstSfWarp);
       uint32_t stage = 0, phase = 0;
       for (int64_t t = unit0; t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, 0);
+        const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, 0);
         bool ok = true;
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           // the stage's previous MMAs finished before its producer refilled it
@@ -928,7 +933,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4>::kThreads, 1)
     const uint32_t tempty_even = mapa_shared(tempty_bar, 0);
     uint32_t acc_phase = 0;
     for (int64_t t = unit0; t < total_units; t += ustride) {
-      const TileInfo ti = map_unit_pair<EPB>(t, p, row_off, prow_off, tile_off, rank);
+      const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
       if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -1017,13 +1022,13 @@ cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const G
   return launch_clusters(kern, Cfg::kThreads, smem, max_units, num_sms, stream, ta, tb, p);
 }
 
-template <int STAGES, bool NVF4>
+template <int STAGES, bool NVF4, int BKB>
 cudaError_t launch_pair_variant(const CUtensorMap& ta, const CUtensorMap& tb,
                                 const CUtensorMap& tsa, const CUtensorMap& tsb,
                                 const GemmParams& p, int64_t max_units, int num_sms,
                                 cudaStream_t stream) {
-  using Cfg = PairCfg<STAGES, NVF4>;
-  auto kern = grouped_gemm_pair_kernel<STAGES, NVF4>;
+  using Cfg = PairCfg<STAGES, NVF4, BKB>;
+  auto kern = grouped_gemm_pair_kernel<STAGES, NVF4, BKB>;
   const size_t smem = Cfg::smem_bytes(p.G);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -1096,19 +1101,20 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.out_cols = mode == 0 ? N : K;
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
-  // default: the CTA-pair kernel (256 x 256 units) whenever a stage is 128
-  // bytes of K and B spans at least the two 128-row bands of one unit
+  // default: the CTA-pair kernel (256 x 256 units) whenever B spans at least
+  // the two 128-row bands of one unit and the stage size is 128 bytes of K
+  // (or 64 bytes with NVFP4)
   if (unaligned && !(BKB == 128 && b_rows >= 256 && !nvfp4)) return cudaErrorInvalidValue;
-  if (unaligned || (tile_n == 0 && !pair && BKB == 128 && b_rows >= 256)) {
+  if (unaligned || (tile_n == 0 && !pair && (BKB == 128 || nvfp4) && b_rows >= 256)) {
     CUtensorMap ta, tb, tsa, tsb;
-    const int atoms = nvfp4 ? 4 : 1;  // scale tiles along K per stage and band
+    const int atoms = nvfp4 ? BKB / 32 : 1;  // scale tiles along K per stage and band
     const uint64_t b_bands = static_cast<uint64_t>(b_rows / 128);
     const uint64_t sfb_dims[3] = {128, static_cast<uint64_t>(p.b_atoms_row), b_bands};
     const uint64_t sfb_strides[2] = {512, static_cast<uint64_t>(512 * p.b_atoms_row)};
     const uint32_t sfb_box[3] = {128, static_cast<uint32_t>(atoms), 2};
     const int64_t ebn = nvfp4 ? 1 : 2;  // bytes per element x 2
-    if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows, 128, 128) ||
-        !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows, 128, 128) ||
+    if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows, 128, BKB) ||
+        !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows, 128, BKB) ||
         !make_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128,
                       static_cast<uint64_t>((a_sf_rows / 128) * p.a_atoms_row), 512, 128,
                       static_cast<uint32_t>(atoms), CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -1116,8 +1122,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
       return cudaErrorInvalidValue;
     const int64_t units = mode == 1 ? G * (((N / 128) + 1) / 2) * ((K + 255) / 256)
                                     : (((M_cap / 128) + G + 1) / 2) * ((p.out_cols + 255) / 256);
-    if (nvfp4) return launch_pair_variant<5, true>(ta, tb, tsa, tsb, p, units, num_sms, stream);
-    return launch_pair_variant<6, false>(ta, tb, tsa, tsb, p, units, num_sms, stream);
+    if (nvfp4 && BKB == 64)
+      return launch_pair_variant<10, true, 64>(ta, tb, tsa, tsb, p, units, num_sms, stream);
+    if (nvfp4) return launch_pair_variant<5, true, 128>(ta, tb, tsa, tsb, p, units, num_sms, stream);
+    return launch_pair_variant<6, false, 128>(ta, tb, tsa, tsb, p, units, num_sms, stream);
   }
 
   const bool pr = pair != 0;

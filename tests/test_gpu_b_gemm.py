@@ -160,6 +160,15 @@ def test_fprop_half_wide_last_column_unit(out_type):
         assert errs.max() <= TOL, errs
 
 
+def test_nvfp4_fprop_k_not_multiple_of_256():
+    # K = 384: 128-byte stages would overrun K, so the pair kernel runs with
+    # 64-byte stages (64-byte swizzle, two MMAs and two scale tiles per band)
+    wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=1024, K=384, N=512, G=4)
+    case, offs, rows, ref = _run_fprop(wl)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
 def test_nvfp4_fprop_half_wide_last_column_unit():
     wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=1024, K=256, N=384, G=4)
     case, offs, rows, ref = _run_fprop(wl)
