@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "mxg_device.cuh"
+#include "mxg_host.h"
 
 namespace mxg {
 
@@ -368,100 +369,155 @@ __global__ void nvfp4_col_zero_kernel(float* __restrict__ outer, int64_t n) {
     outer[i] = 0.0f;
 }
 
-// Thread (column pair cp, 32-row quarter j) of a 128 x 128 tile.
-__global__ void __launch_bounds__(256)
-    nvfp4_col_amax_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
-                          const int64_t* __restrict__ ws, int G, float* __restrict__ outer) {
-  extern __shared__ int64_t row_off[];
-  const int Gt = ws ? G : 1;
-  if (threadIdx.x < 32) build_row_offsets(ws, G, cap, row_off);
-  __syncthreads();
-  const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
-  const uint32_t cp = threadIdx.x & 63u, j = threadIdx.x >> 6;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
-    const int g = group_of_row(row_off, Gt, m0);
-    const uint32_t* col = reinterpret_cast<const uint32_t*>(x + (m0 + 32 * j) * cols + k0) + cp;
-    float alo = 0.f, ahi = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t w = col[i * (cols >> 1)];
-      alo = fmaxf(alo, fabsf(bf16lo(w)));
-      ahi = fmaxf(ahi, fabsf(bf16hi(w)));
-    }
-    unsigned int* o = reinterpret_cast<unsigned int*>(outer + static_cast<int64_t>(g) * cols + k0 + 2 * cp);
-    atomicMax(o, __float_as_uint(alo));  // non-negative floats order as their bits
-    atomicMax(o + 1, __float_as_uint(ahi));
-  }
-}
+// The two passes over 128 x 128 bf16 tiles, staged in shared memory by TMA
+// (double buffered: thread 0 loads the CTA's next tile while all threads work
+// on the current one).  Thread (column pair cp, 32-row quarter j); a 32-bit
+// word of the tile holds columns 2cp and 2cp+1 of one row.  A tile lies in
+// one group (groups are multiples of 128 rows).
+//   AMAX:  column amax over the tile (packed bf16 maximum, both columns at
+//          once), reduced over the four quarters in shared memory, folded into
+//          outer[g, k] with atomicMax on the float bits (non-negative floats
+//          order as integers, so the result does not depend on the order).
+//   QUANT: the 16-row blocks of each column with the group's column amax,
+//          written transposed (16 bytes per column and quarter), scales staged
+//          and stored as two 512-byte swizzle tiles.
+constexpr int kNvColTileBytes = 128 * 128 * 2;
+// dynamic shared memory: two tiles, alignment slack, then the G + 1 row offsets
+constexpr int kNvColSmem = 2 * kNvColTileBytes + 1024;
 
-__global__ void __launch_bounds__(256)
-    nvfp4_col_quant_kernel(const uint16_t* __restrict__ x, int64_t cap, int64_t cols,
-                           const int64_t* __restrict__ ws, int G, const float* __restrict__ amax,
+template <bool QUANT>
+__global__ void __launch_bounds__(256, 3)
+    nvfp4_col_tiles_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
+                           const int64_t* __restrict__ ws, int G, float* __restrict__ outer,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT) {
-  extern __shared__ int64_t row_off[];
+  extern __shared__ uint8_t csm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(csm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bars[2];
+  __shared__ int abort_s;
+  __shared__ float part[4][128];
   __shared__ __align__(16) uint8_t sf_s[2][512];
+  int64_t* row_off = reinterpret_cast<int64_t*>(sm + 2 * kNvColTileBytes);
   const int Gt = ws ? G : 1;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    abort_s = 0;
+    fence_barrier_init();
+  }
   if (threadIdx.x < 32) build_row_offsets(ws, G, cap, row_off);
   __syncthreads();
+  volatile int* abort_flag = &abort_s;
   const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
+  auto issue = [&](int64_t t, int b) {
+    const uint32_t bar = smem_u32(&bars[b]);
+    mbar_arrive_expect_tx(bar, kNvColTileBytes);
+    tma_load_2d(smem_u32(sm + b * kNvColTileBytes), &tmap_x, bar,
+                static_cast<int32_t>((t % kt) << 7), static_cast<int32_t>((t / kt) << 7));
+  };
+  if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
+    prefetch_tmap(&tmap_x);
+    issue(blockIdx.x, 0);
+  }
   const uint32_t cp = threadIdx.x & 63u, j = threadIdx.x >> 6;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+  uint32_t parity = 0u, pending = static_cast<int64_t>(blockIdx.x) < tiles ? 1u : 0u;
+  int b = 0;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, b ^= 1) {
+    if (threadIdx.x == 0 && t + gridDim.x < tiles) {
+      issue(t + gridDim.x, b ^ 1);
+      pending |= 1u << (b ^ 1);
+    }
+    if (!mbar_wait(smem_u32(&bars[b]), (parity >> b) & 1u, abort_flag, nullptr)) *abort_flag = 1;
+    parity ^= 1u << b;
+    pending &= ~(1u << b);
+    __syncthreads();
+    if (*abort_flag) break;
     const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
     const int g = group_of_row(row_off, Gt, m0);
-    const uint32_t* col = reinterpret_cast<const uint32_t*>(x + (m0 + 32 * j) * cols + k0) + cp;
-    uint32_t w[32];
+    const uint32_t* col = reinterpret_cast<const uint32_t*>(sm + b * kNvColTileBytes) +
+                          (32 * j) * 64 + cp;
+    if (!QUANT) {
+      uint32_t m = 0;
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) m = bf16x2_max_abs(m, col[i * 64]);
+      part[j][2 * cp] = __uint_as_float((m & 0x7FFFu) << 16);
+      part[j][2 * cp + 1] = __uint_as_float(m & 0x7FFF0000u);
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const uint32_t c = threadIdx.x;
+        const float a = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
+        atomicMax(reinterpret_cast<unsigned int*>(outer + static_cast<int64_t>(g) * cols + k0 + c),
+                  __float_as_uint(a));
+      }
+    } else {
+      uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = col[i * (cols >> 1)];
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t kk = 2 * cp + c;
-      const float A = amax[static_cast<int64_t>(g) * cols + k0 + kk];
-      const bool zero = !(A > 0.f);
-      const float S = zero ? 0.f : __fdiv_rn(2688.0f, A);
-      uint32_t o[4];
+      for (int i = 0; i < 32; ++i) w[i] = col[i * 64];
+      // 16-row block amax of both columns at once (packed bf16 maximum)
+      uint32_t bm[2];
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        float ab = 0.f;
+        uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          ab = fmaxf(ab, fabsf(c ? bf16hi(w[16 * blk + i]) : bf16lo(w[16 * blk + i])));
-        uint32_t sbyte = 0;
-        if (!zero) sbyte = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ab, 6.0f), S), 0.f) & 0x7Fu;
-        const float sbv = ue4m3_value(sbyte);
-        const float ratio = sbv == 0.f ? 0.f : __fdiv_rn(S, sbv);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {  // byte i: rows 2i (low nibble), 2i+1 of this 8-row run
-            const int r = 16 * blk + 8 * h + 2 * i;
-            const float v0 = c ? bf16hi(w[r]) : bf16lo(w[r]);
-            const float v1 = c ? bf16hi(w[r + 1]) : bf16lo(w[r + 1]);
-            uint32_t byte;
-            if (sbv == 0.f) {
-              byte = (signbit(v0) ? 0x8u : 0u) | (signbit(v1) ? 0x80u : 0u);
-            } else {
-              byte = cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio));
-            }
-            word |= byte << (8 * i);
-          }
-          o[2 * blk + h] = word;
-        }
-        const uint32_t sc = 2 * j + blk;  // scale column within the tile (0..7)
-        sf_s[sc >> 2][(kk & 31u) * 16 + (kk >> 5) * 4 + (sc & 3u)] = static_cast<uint8_t>(sbyte);
+        for (int i = 0; i < 16; ++i) m = bf16x2_max_abs(m, w[16 * blk + i]);
+        bm[blk] = m;
       }
-      *reinterpret_cast<uint4*>(qT + (k0 + kk) * (cap >> 1) + ((m0 + 32 * j) >> 1)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t kk = 2 * cp + c;
+        const float A = outer[static_cast<int64_t>(g) * cols + k0 + kk];
+        const bool zero = !(A > 0.f);
+        const float S = zero ? 0.f : __fdiv_rn(2688.0f, A);
+        uint32_t o[4];
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const float ab = c ? __uint_as_float(bm[blk] & 0x7FFF0000u)
+                             : __uint_as_float((bm[blk] & 0x7FFFu) << 16);
+          uint32_t sbyte = 0;
+          if (!zero) sbyte = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ab, 6.0f), S), 0.f) & 0x7Fu;
+          const float sbv = ue4m3_value(sbyte);
+          const float ratio = sbv == 0.f ? 0.f : __fdiv_rn(S, sbv);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {  // byte i: rows 2i (low nibble), 2i+1 of this 8-row run
+              const int r = 16 * blk + 8 * h + 2 * i;
+              const float v0 = c ? bf16hi(w[r]) : bf16lo(w[r]);
+              const float v1 = c ? bf16hi(w[r + 1]) : bf16lo(w[r + 1]);
+              uint32_t byte;
+              if (sbv == 0.f) {
+                byte = (signbit(v0) ? 0x8u : 0u) | (signbit(v1) ? 0x80u : 0u);
+              } else {
+                byte = cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio));
+              }
+              word |= byte << (8 * i);
+            }
+            o[2 * blk + h] = word;
+          }
+          const uint32_t sc = 2 * j + blk;  // scale column within the tile (0..7)
+          sf_s[sc >> 2][(kk & 31u) * 16 + (kk >> 5) * 4 + (sc & 3u)] = static_cast<uint8_t>(sbyte);
+        }
+        *reinterpret_cast<uint4*>(qT + (k0 + kk) * (cap >> 1) + ((m0 + 32 * j) >> 1)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      __syncthreads();
+      if (threadIdx.x < 64) {
+        const uint32_t a = threadIdx.x >> 5, l = threadIdx.x & 31u;
+        const int64_t atom = (k0 >> 7) * (cap >> 6) + (m0 >> 6) + a;
+        reinterpret_cast<uint4*>(sfT + atom * 512)[l] = reinterpret_cast<const uint4*>(sf_s[a])[l];
+      }
     }
-    __syncthreads();
-    if (threadIdx.x < 64) {
-      const uint32_t a = threadIdx.x >> 5, l = threadIdx.x & 31u;
-      const int64_t atom = (k0 >> 7) * (cap >> 6) + (m0 >> 6) + a;
-      reinterpret_cast<uint4*>(sfT + atom * 512)[l] = reinterpret_cast<const uint4*>(sf_s[a])[l];
-    }
-    __syncthreads();
+    __syncthreads();  // tile buffer, part[] and the scale staging are reused
   }
+  // a prefetch still in flight (only after an abort) lands before the CTA exits
+  if (threadIdx.x == 0)
+    for (int bb = 0; bb < 2; ++bb)
+      if (pending & (1u << bb)) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(smem_u32(&bars[bb]), (parity >> bb) & 1u))
+          if (globaltimer() - t0 > kWaitTimeoutNs) break;
+      }
 }
 
 __global__ void nvfp4_col_finalize_kernel(float* __restrict__ outer, int64_t n) {
@@ -483,11 +539,30 @@ cudaError_t launch_nvfp4_quantize_colwise(const uint16_t* x, int64_t cap, int64_
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || cap == 0) return e;
   const int64_t max_tiles = (cap >> 7) * (cols >> 7);
-  const int grid = static_cast<int>(std::min<int64_t>(max_tiles, num_sms * 4));
-  const size_t smem = sizeof(int64_t) * (Gt + 1);
-  nvfp4_col_amax_kernel<<<grid, 256, smem, stream>>>(x, cap, cols, group_ws, G, outer);
+  CUtensorMap tm;
+  if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, static_cast<uint64_t>(cols),
+                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  auto ka = nvfp4_col_tiles_kernel<false>;
+  auto kq = nvfp4_col_tiles_kernel<true>;
+  const int smem = kNvColSmem + 8 * (Gt + 1);
+  if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+          cudaSuccess ||
+      (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+          cudaSuccess)
+    return e;
+  // persistent grids: as many CTAs as are resident at once
+  auto grid_of = [&](auto kern) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    return static_cast<int>(std::min<int64_t>(max_tiles, static_cast<int64_t>(num_sms) * per_sm));
+  };
+  ka<<<grid_of(ka), 256, smem, stream>>>(tm, cap, cols, group_ws, G, outer, qT, sfT);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  nvfp4_col_quant_kernel<<<grid, 256, smem, stream>>>(x, cap, cols, group_ws, G, outer, qT, sfT);
+  kq<<<grid_of(kq), 256, smem, stream>>>(tm, cap, cols, group_ws, G, outer, qT, sfT);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   nvfp4_col_finalize_kernel<<<gz, 256, 0, stream>>>(outer, n_outer);
   return cudaGetLastError();
