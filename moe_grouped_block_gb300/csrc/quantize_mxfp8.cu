@@ -166,7 +166,7 @@ constexpr int kQSmemBytes = 2 * kQTileBytes + 2 * 512 + 2 * 8 + 16 + 1024;
 // row offset in sf_row, q_col and sf_col; cap_col is the row count of the
 // colwise copy (cap, or cap + 128 G when padded).
 template <bool ROW, bool COL, bool UNA>
-__global__ void __launch_bounds__(256, UNA ? 2 : 3)
+__global__ void __launch_bounds__(256, 3)
     mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                           const int64_t* __restrict__ group_ws, int G, uint8_t* __restrict__ q_row,
                           uint8_t* __restrict__ sf_row, uint8_t* __restrict__ q_col,
@@ -363,11 +363,16 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
                     CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const int smem = kQSmemBytes + (unaligned ? 12 * (G + 1) + 16 : 0);
-  const int64_t per_sm = smem <= 75 * 1024 ? 3 : 2;
-  const int grid = static_cast<int>(max_tiles < num_sms * per_sm ? max_tiles : num_sms * per_sm);
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // persistent grid: as many CTAs as are resident at once
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    const int64_t full = static_cast<int64_t>(num_sms) * per_sm;
+    const int grid = static_cast<int>(max_tiles < full ? max_tiles : full);
     const int qcol_v8 = (reinterpret_cast<uintptr_t>(q_col) & 31u) == 0 ? 1 : 0;
     kern<<<grid, 256, smem, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col, sf_col,
                                        qcol_v8, cap_col, status);
