@@ -409,11 +409,15 @@ __global__ void __launch_bounds__(256, 3)
   __syncthreads();
   volatile int* abort_flag = &abort_s;
   const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
+  // the QUANT pass walks the tiles in the reverse order of the AMAX pass, so
+  // that it starts on the tiles the AMAX pass read last, still held in L2
+  auto tile_of = [&](int64_t t) { return QUANT ? tiles - 1 - t : t; };
   auto issue = [&](int64_t t, int b) {
     const uint32_t bar = smem_u32(&bars[b]);
+    const int64_t tt = tile_of(t);
     mbar_arrive_expect_tx(bar, kNvColTileBytes);
     tma_load_2d(smem_u32(sm + b * kNvColTileBytes), &tmap_x, bar,
-                static_cast<int32_t>((t % kt) << 7), static_cast<int32_t>((t / kt) << 7));
+                static_cast<int32_t>((tt % kt) << 7), static_cast<int32_t>((tt / kt) << 7));
   };
   if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
     prefetch_tmap(&tmap_x);
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(256, 3)
     pending &= ~(1u << b);
     __syncthreads();
     if (*abort_flag) break;
-    const int64_t m0 = (t / kt) << 7, k0 = (t % kt) << 7;
+    const int64_t tt = tile_of(t), m0 = (tt / kt) << 7, k0 = (tt % kt) << 7;
     const int g = group_of_row(row_off, Gt, m0);
     const uint32_t* col = reinterpret_cast<const uint32_t*>(sm + b * kNvColTileBytes) +
                           (32 * j) * 64 + cp;

@@ -100,9 +100,10 @@ class tile_n:
 
 
 def fprop_case(wl: workloads.Workload, layout_x=mxg.MXG_ROWWISE, out_type=mxg.MXG_OUT_F32,
-               alpha=None, beta=None, c_in=None, fill_c=0.0, bias=None):
+               alpha=None, beta=None, c_in=None, fill_c=0.0, bias=None, c_offset=0):
     """Quantize x and w and run the fprop GEMM on the GPU.  Returns a dict of
-    host inputs, device outputs and the offsets."""
+    host inputs, device outputs and the offsets.  With c_offset > 0, C starts
+    c_offset elements into a larger buffer (returned as "C_buf")."""
     inp = workloads.make_inputs(wl)
     G, N, K, R = wl.G, wl.N, wl.K, wl.rows_capacity
     x = inp["x"].to(DEV)
@@ -120,18 +121,18 @@ def fprop_case(wl: workloads.Workload, layout_x=mxg.MXG_ROWWISE, out_type=mxg.MX
         A = (qx["q_row"], qx["sf_row"], qx["outer_row"])
         B = (qw["q_row"], qw["sf_row"], qw["outer_row"])
     cdt = torch.float32 if out_type == mxg.MXG_OUT_F32 else torch.bfloat16
+    C_buf = torch.full((c_offset + R * N,), fill_c, dtype=cdt, device=DEV)
+    C = C_buf[c_offset:].view(R, N)
     if c_in is not None:
-        C = c_in.to(DEV, cdt).clone()
-    else:
-        C = torch.full((R, N), fill_c, dtype=cdt, device=DEV)
+        C.copy_(c_in.to(DEV, cdt))
     al = None if alpha is None else torch.tensor(alpha, dtype=torch.float32, device=DEV)
     be = None if beta is None else torch.tensor(beta, dtype=torch.float32, device=DEV)
     bi = None if bias is None else torch.as_tensor(bias, dtype=torch.float32).to(DEV)
     mxg.mxg_grouped_gemm(fmt, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, al, be, C, out_type,
                          dev_status=st, bias=bi)
     torch.cuda.synchronize()
-    return {"inp": inp, "ws": ws, "status": st, "qx": qx, "qw": qw, "C": C, "G": G, "N": N,
-            "K": K, "R": R}
+    return {"inp": inp, "ws": ws, "status": st, "qx": qx, "qw": qw, "C": C, "C_buf": C_buf,
+            "G": G, "N": N, "K": K, "R": R}
 
 
 def oracle_quantized_operands(wl: workloads.Workload, inp: dict):

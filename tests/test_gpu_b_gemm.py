@@ -144,6 +144,31 @@ def test_fprop_bf16_output(tn):
 
 
 @pytest.mark.parametrize("out_type", [mxg.MXG_OUT_F32, mxg.MXG_OUT_BF16])
+@pytest.mark.parametrize("c_offset_bytes", [0, 16])
+def test_fprop_stores_stay_in_bounds(out_type, c_offset_bytes):
+    # C starts 16 (not 32) bytes into its buffer in one case (16-byte stores
+    # instead of whole-sector ones), the buffer has 256 spare capacity rows,
+    # and the Dirichlet sizes put group ends inside the CTA-pair units: every
+    # row < M matches the oracle and nothing else in the buffer (the prefix,
+    # the capacity rows) changes from the sentinel.
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=2048, K=256, N=512, M_cap=2304)
+    esize = 4 if out_type == mxg.MXG_OUT_F32 else 2
+    sentinel = 7.0
+    case, offs, rows, ref = _run_fprop(wl, out_type=out_type, fill_c=sentinel,
+                                       c_offset=c_offset_bytes // esize)
+    buf = case["C_buf"].cpu().float().numpy().astype(np.float64)
+    assert np.all(buf[:c_offset_bytes // esize] == sentinel)
+    got = case["C"].cpu().float().numpy().astype(np.float64)
+    assert np.all(got[wl.M:] == sentinel)
+    if out_type == mxg.MXG_OUT_BF16:
+        refb = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        assert np.all(np.abs(got[:wl.M] - refb) <= np.abs(refb) * 2.0 ** -7 + 1e-6 * np.abs(ref).max())
+    else:
+        errs = normwise_errors(got[:wl.M], ref, offs)
+        assert errs.max() <= TOL, errs
+
+
+@pytest.mark.parametrize("out_type", [mxg.MXG_OUT_F32, mxg.MXG_OUT_BF16])
 def test_fprop_half_wide_last_column_unit(out_type):
     # N = 384: the CTA-pair kernel's last 256-wide column unit is half wide; its
     # upper 128 columns (the next expert's weight rows, or the zero fill past
