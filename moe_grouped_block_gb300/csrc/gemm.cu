@@ -632,9 +632,9 @@ struct PairCfg {
   static constexpr int kTmemCols = 512;
   static_assert(BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
   static constexpr int kSfCopies = 3 * kAtomsK;  // scale tiles per stage (A, then B bands)
-  // full[S], empty[S], sfready[S], sffull[S], tfull, tempty, drain, sfdrain;
+  // full[S], empty[S], sffull[S], tfull, tempty, drain, sfdrain;
   // TMEM base; abort flag
-  static constexpr int kBarBytes = 8 * (4 * STAGES + 4) + 16;
+  static constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
   static size_t smem_bytes(int G) {
     return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16;
   }
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (4 * STAGES + 4));
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * STAGES + 4));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
@@ -726,20 +726,20 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-  auto sfready_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + s]); };
-  auto sffull_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + s]); };
-  const uint32_t tfull_bar = smem_u32(&bars[4 * STAGES]);
-  const uint32_t tempty_bar = smem_u32(&bars[4 * STAGES + 1]);
-  const uint32_t drain_bar = smem_u32(&bars[4 * STAGES + 2]);
-  const uint32_t sfdrain_bar = smem_u32(&bars[4 * STAGES + 3]);
+  auto sffull_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + s]); };
+  const uint32_t tfull_bar = smem_u32(&bars[3 * STAGES]);
+  const uint32_t tempty_bar = smem_u32(&bars[3 * STAGES + 1]);
+  const uint32_t drain_bar = smem_u32(&bars[3 * STAGES + 2]);
+  const uint32_t sfdrain_bar = smem_u32(&bars[3 * STAGES + 3]);
   constexpr uint32_t kFirstSfWarp = 2 + Cfg::kEpiWarps;
 
   // ------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);   // even CTA: its producer's arrival + both CTAs' bytes
+      // even CTA: its producer's arrival + both CTAs' bytes + the scale-copy
+      // warps' commits (scale tiles in tensor memory)
+      mbar_init(full_bar(s), 1 + Cfg::kSfWarps);
       mbar_init(empty_bar(s), 1);  // the pair's MMA commit
-      mbar_init(sfready_bar(s), Cfg::kSfWarps);  // even CTA: the scale-copy warps' commits
       mbar_init(sffull_bar(s), 1);  // even CTA: its producer's arrival + both CTAs' scale bytes
     }
     mbar_init(tfull_bar, 1);
@@ -836,8 +836,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
         tc_fence_after();
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           // operands landed, and their scale tiles are in tensor memory
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns) ||
-              !mbar_wait(sfready_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -912,7 +911,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
                                 smem_desc(ssfb + i * 512 * Cfg::kAtomsK + 512 * a, 0, 128, 0));
             }
           }
-          tc_commit_pair(sfready_bar(stage));
+          // one of the full barrier's arrivals: the MMA thread waits there for
+          // the operand bytes and these scale copies alike
+          tc_commit_pair(full_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
