@@ -84,10 +84,11 @@ int env_tile_n() {
   return s ? std::atoi(s) : 0;
 }
 
-// Bytes of K per GEMM pipeline stage: 128 (default) or 64.
+// Bytes of K per GEMM pipeline stage: 0 (default: 256 for MXFP8 fprop on the
+// CTA-pair kernel when K % 256 == 0, else 128), 128 or 64.
 int env_bk() {
   const char* s = std::getenv("MXG_GEMM_BK");
-  return s ? std::atoi(s) : 128;
+  return s ? std::atoi(s) : 0;
 }
 
 // L2 prefetch distance of the GEMM producer, in K blocks (default off: on

@@ -276,7 +276,27 @@ def test_nvfp4_fprop_alpha():
 @pytest.mark.parametrize("tn,K", [(None, 512), (None, 384), (256, 512), (128, 256)])
 def test_dgrad_scaled(tn, K):
     """dX = dY . W_g: rowwise dY, colwise (transposed) copy of W."""
-    wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=2048, K=K, N=256, G=8)
+    _dgrad_check(tn, K, 256)
+
+
+@pytest.mark.parametrize("N", [384, 512, 768])
+@pytest.mark.parametrize("bk", [None, "128"])
+def test_stage_width_fprop_and_dgrad(N, bk, monkeypatch):
+    """The MXFP8 CTA-pair kernel takes 256 bytes of K per fprop stage when K
+    is a multiple of 256 and 128 otherwise (or when MXG_GEMM_BK=128 forces it);
+    dgrad keeps 128.  Both widths, with one and several stages, and dgrad over
+    the same contraction lengths, match the oracle."""
+    if bk is not None:
+        monkeypatch.setenv("MXG_GEMM_BK", bk)
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=N, N=512)
+    case, offs, rows, ref = _run_fprop(wl)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+    _dgrad_check(None, 512, N)
+
+
+def _dgrad_check(tn, K, N):
+    wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=2048, K=K, N=N, G=8)
     inp = workloads.make_inputs(wl)
     G, N, M = wl.G, wl.N, wl.M
     dy_h = workloads.random_bf16((M, N), seed=71, scale=1e-3)
