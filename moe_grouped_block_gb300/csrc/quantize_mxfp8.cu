@@ -154,11 +154,11 @@ __device__ __forceinline__ float abs_hi(uint32_t m) { return __uint_as_float(m &
 
 }  // namespace
 
-// Shared memory: two 32 KB bf16 tiles (TMA double buffer), two 512-byte scale
-// staging tiles, two mbarriers, the live-row count and the abort flag; with
-// unaligned groups, three int32 tables of G + 1 entries after them.
+// Shared memory: two 32 KB bf16 tiles (TMA double buffer), two mbarriers, the
+// live-row count and the abort flag; with unaligned groups, three int32
+// tables of G + 1 entries after them.
 constexpr int kQTileBytes = 128 * 128 * 2;
-constexpr int kQSmemBytes = 2 * kQTileBytes + 2 * 512 + 2 * 8 + 16 + 1024;
+constexpr int kQSmemBytes = 2 * kQTileBytes + 2 * 8 + 16 + 1024;
 
 // UNA: group sizes of any value.  Tiles are then 128-row tiles of each group
 // (the last one may extend past the group: those rows are zeroed in shared
@@ -175,9 +175,7 @@ __global__ void __launch_bounds__(256, 3)
   extern __shared__ uint8_t qsmem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* sfr_s = sm + 2 * kQTileBytes;
-  uint8_t* sfc_s = sfr_s + 512;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sfc_s + 512);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 2 * kQTileBytes);
   int64_t* live_s = reinterpret_cast<int64_t*>(bars + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(live_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(live_s + 2);  // UNA only
@@ -242,17 +240,20 @@ __global__ void __launch_bounds__(256, 3)
   uint32_t parity = 0u;  // bit b: phase parity of buffer b
   uint32_t pending = static_cast<int64_t>(blockIdx.x) < tiles ? 1u : 0u;  // thread 0's loads
   int b = 0;
+  // One __syncthreads per tile: once every thread has passed it, the previous
+  // tile's buffer is no longer read, so thread 0 refills it with the tile
+  // after this one; the scale bytes go straight to their swizzled positions in
+  // global memory (no staging, no second barrier).
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, b ^= 1) {
-    // the other buffer was released by the __syncthreads ending the previous tile
-    if (threadIdx.x == 0 && t + gridDim.x < tiles) {
-      issue(t + gridDim.x, b ^ 1);
-      pending |= 1u << (b ^ 1);
-    }
     if (!mbar_wait(smem_u32(&bars[b]), (parity >> b) & 1u, abort_flag, status)) *abort_flag = 1;
     parity ^= 1u << b;
     pending &= ~(1u << b);
     __syncthreads();
     if (*abort_flag) break;
+    if (threadIdx.x == 0 && t + gridDim.x < tiles) {
+      issue(t + gridDim.x, b ^ 1);
+      pending |= 1u << (b ^ 1);
+    }
 
     const RowTile rtl = row_tile(t / kt);
     const int64_t m0 = rtl.m0, mp = rtl.mp, k0 = (t % kt) << 7;
@@ -268,6 +269,7 @@ __global__ void __launch_bounds__(256, 3)
 
     // ---- phase 1: rows (16 lanes per row, 16-byte chunks; conflict-free per 8-lane phase)
     if (ROW) {
+      uint8_t* sfr = sf_row + ((mp >> 7) * kt + (k0 >> 7)) * 512;  // this tile's scale tile
 #pragma unroll 4
       for (int i = 0; i < 8; ++i) {
         const uint32_t r = i * 16 + warp * 2 + half;
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(256, 3)
         if (!UNA || static_cast<int>(r) < rtl.valid)
           *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
         if ((cl & 3u) == 0)
-          sfr_s[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
+          sfr[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
       }
     }
 
@@ -321,22 +323,10 @@ __global__ void __launch_bounds__(256, 3)
         reinterpret_cast<uint4*>(dhi)[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
       }
       const uint32_t klo = 2 * cp, khi = klo + 1;
-      sfc_s[(klo & 31u) * 16 + (klo >> 5) * 4 + j] = static_cast<uint8_t>(elo + 127);
-      sfc_s[(khi & 31u) * 16 + (khi >> 5) * 4 + j] = static_cast<uint8_t>(ehi + 127);
+      uint8_t* sfc = sf_col + ((k0 >> 7) * (cap_col >> 7) + (mp >> 7)) * 512;
+      sfc[(klo & 31u) * 16 + (klo >> 5) * 4 + j] = static_cast<uint8_t>(elo + 127);
+      sfc[(khi & 31u) * 16 + (khi >> 5) * 4 + j] = static_cast<uint8_t>(ehi + 127);
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      if (ROW) {
-        const int64_t atom = (mp >> 7) * kt + (k0 >> 7);
-        reinterpret_cast<uint4*>(sf_row + atom * 512)[threadIdx.x] =
-            reinterpret_cast<const uint4*>(sfr_s)[threadIdx.x];
-      }
-    } else if (COL && threadIdx.x < 64) {
-      const int64_t atom = (k0 >> 7) * (cap_col >> 7) + (mp >> 7);
-      reinterpret_cast<uint4*>(sf_col + atom * 512)[threadIdx.x - 32] =
-          reinterpret_cast<const uint4*>(sfc_s)[threadIdx.x - 32];
-    }
-    __syncthreads();  // tile buffer and scale staging are reused
   }
   // a prefetch still in flight (only after an abort) lands before the CTA exits
   if (threadIdx.x == 0)
