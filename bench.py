@@ -399,6 +399,35 @@ def measure_e2e(path, step, args, dist, dev, flush, stream):
     return ms, h2d, d2h
 
 
+def gemm_roofline(gemm_name, flops, gemm_bytes, gemm_ms, peaks, peak_src, nvfp4, traffic):
+    """The roofline object of the GEMM launch.  Its roofline time is the larger
+    of its algorithmic FLOP at the dense tensor peak (measured bf16 x 2 for
+    MXFP8, x 6 for NVFP4: the nominal ratios) and its algorithmic bytes at the
+    measured HBM bandwidth; that one names the bound (HBM for the row-scaled
+    NVFP4 layer, tensor for the others) and sets achieved / peak / frac."""
+    peak_tc = peaks["bf16_tflops"] * (6.0 if nvfp4 else 2.0)
+    tflops = flops / (gemm_ms * 1e-3) / 1e12
+    t_tensor_ms = flops / (peak_tc * 1e12) * 1e3
+    t_hbm_ms = gemm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    common = {"kernel": gemm_name,
+              "peak_source": "%s bf16_tflops (burst) x %d; %s hbm_gbs" % (
+                  peak_src, 6 if nvfp4 else 2, peak_src),
+              "traffic": traffic,
+              "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size "
+                                "launch (profiles/grouped_gemm_pair_kernel_dram_traffic.md); "
+                                "null when the kernel changed since",
+              "algorithmic_bytes": gemm_bytes, "algorithmic_flop": flops,
+              "t_tensor_roofline_ms": round(t_tensor_ms, 5), "t_hbm_roofline_ms": round(t_hbm_ms, 5),
+              "t_roofline_over_t": round(max(t_tensor_ms, t_hbm_ms) / gemm_ms, 4)}
+    if t_hbm_ms > t_tensor_ms:
+        gbs = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "tflops": round(tflops, 1), "tflops_frac": round(tflops / peak_tc, 4), **common}
+    return {"bound": "tensor", "achieved": round(tflops, 1), "peak": round(peak_tc, 1),
+            "unit": "TFLOP/s", "frac": round(tflops / peak_tc, 4), **common}
+
+
 def run_mxg(args, wl, ws_world, rank, local):
     import torch
     from moe_grouped_block_gb300 import mxg
@@ -474,21 +503,8 @@ def run_mxg(args, wl, ws_world, rank, local):
     gemm_name = [n for n in per_kernel if n.startswith("grouped_gemm")][0]
     gemm_ms = float(np.mean(per_kernel[gemm_name]))
     nvfp4 = wl.fmt == "nvfp4"
-    # dense MXFP8 peak = measured bf16 peak x 2 (nominal fp8 : bf16 ratio);
-    # NVFP4 x 6 (nominal 13.5 : 2.25)
-    peak_tc = peaks["bf16_tflops"] * (6.0 if nvfp4 else 2.0)
-    achieved = flops / (gemm_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": gemm_name, "achieved": round(achieved, 1),
-                "peak": round(peak_tc, 1), "unit": "TFLOP/s", "frac": round(achieved / peak_tc, 4),
-                "peak_source": "%s bf16_tflops (burst) x %d" % (peak_src, 6 if nvfp4 else 2),
-                "traffic": measured_traffic(wl.name),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size "
-                                  "launch (profiles/grouped_gemm_pair_kernel_dram_traffic.md); "
-                                  "null when the kernel changed since"}
-    if nvfp4:  # the NVFP4 layer is HBM-bound: report the time roofline too
-        b = path.kernel_bytes(gemm_name)
-        roofline["hbm_bytes"] = b
-        roofline["t_hbm_roofline_ms"] = round(b / (peaks["hbm_gbs"] * 1e9) * 1e3, 5)
+    roofline = gemm_roofline(gemm_name, flops, path.kernel_bytes(gemm_name), gemm_ms, peaks,
+                             peak_src, nvfp4, measured_traffic(wl.name))
     value = job_tflops(flops, ws_world, ms)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_world,

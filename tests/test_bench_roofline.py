@@ -1,0 +1,52 @@
+"""Host logic of the benchmark's GEMM roofline object (no GPU): the bound is
+whichever roofline time is larger, FLOP at the dense tensor peak or
+algorithmic bytes at the measured HBM bandwidth, and frac is the achieved
+fraction of that peak, equal to t_roofline / t."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+PEAKS = {"bf16_tflops": 1892.9, "hbm_gbs": 6776.3}
+
+
+def test_mixtral_fprop_is_tensor_bound():
+    # 2 M N K FLOP; A + W of the live experts (+ scales) + bf16 C
+    M, N, K, G = 16384, 14336, 4096, 8
+    flops = 2.0 * M * N * K
+    nbytes = M * K * (1 + 1 / 32) + G * N * K * (1 + 1 / 32) + M * N * 2
+    r = bench.gemm_roofline("g", flops, nbytes, 0.6, PEAKS, "measured", False, None)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["peak"] == pytest.approx(2 * 1892.9, rel=1e-4)
+    assert r["achieved"] == pytest.approx(flops / 0.6e-3 / 1e12, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["t_roofline_over_t"], rel=1e-3)
+
+
+def test_rowscaled_nvfp4_layer_is_hbm_bound():
+    # 32 experts, K 7168, N 2048, M 16384 (all experts live), bf16 C: the
+    # algorithmic bytes take longer at HBM bandwidth than the FLOP at the NVFP4 peak
+    M, N, K, G = 16384, 2048, 7168, 32
+    flops = 2.0 * M * N * K
+    nbytes = M * K * (0.5 + 1 / 16) + G * N * K * (0.5 + 1 / 16) + M * N * 2 + 4 * (M + G * N)
+    t = 0.1105
+    r = bench.gemm_roofline("g", flops, nbytes, t, PEAKS, "measured", True, 123)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == PEAKS["hbm_gbs"]
+    assert r["t_hbm_roofline_ms"] > r["t_tensor_roofline_ms"]
+    assert r["frac"] == pytest.approx(nbytes / (PEAKS["hbm_gbs"] * 1e9) / (t * 1e-3), rel=1e-3)
+    assert r["frac"] == pytest.approx(r["t_roofline_over_t"], rel=1e-3)
+    assert r["tflops_frac"] == pytest.approx(flops / (t * 1e-3) / 1e12 / (6 * 1892.9), rel=1e-3)
+    assert r["traffic"] == 123
+
+
+def test_finegrained_sits_just_on_the_tensor_side():
+    # G 64, K 2048, N 1408, M 32768: near the ridge, the FLOP time is the larger
+    M, N, K = 32768, 1408, 2048
+    flops = 2.0 * M * N * K
+    live = 43
+    nbytes = M * K * (1 + 1 / 32) + live * N * K * (1 + 1 / 32) + M * N * 2
+    r = bench.gemm_roofline("g", flops, nbytes, 0.0924, PEAKS, "measured", False, None)
+    assert r["bound"] == "tensor"
+    assert r["t_tensor_roofline_ms"] > r["t_hbm_roofline_ms"]
