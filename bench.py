@@ -119,17 +119,68 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """SM clock and clock-event reasons during the timed region.  Reads NVML
+    (the driver's libnvidia-ml, through ctypes) every millisecond on a thread
+    between start() and stop(); the device is found by the CUDA device's UUID.
+    Without NVML it falls back to nvidia-smi every 200 ms.  Read-only: no
+    setting of the GPU is changed."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason* bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid=None):
         self.idx = gpu_index
+        self.uuid = uuid
         self.proc = None
         self.lines = []
+        self.nvml = None
+        self.samples = []
+        self.running = False
+
+    def _nvml_handle(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(("GPU-%s" % self.uuid).encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.idx), ctypes.byref(h)) == 0
+        if not ok:
+            return None
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, h, reasons_fn
+
+    def _poll(self):
+        import ctypes
+        lib, h, reasons_fn = self.nvml
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while self.running:
+            if (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and   # NVML_CLOCK_SM
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    reasons_fn(h, ctypes.byref(rs)) == 0):
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(0.001)
 
     def start(self):
+        try:
+            self.nvml = self._nvml_handle()
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.running = True
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
@@ -137,6 +188,7 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            time.sleep(0.3)
         except OSError:
             self.proc = None
 
@@ -145,6 +197,14 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml is not None:
+            self.running = False
+            self.t.join(timeout=2)
+            sm = [c for c, _, _ in self.samples]
+            reasons = {n for _, _, r in self.samples for n, b in self.REASON_BITS.items() if r & b}
+            return {"sm_mhz": statistics.median(sm) if sm else None,
+                    "sm_max_mhz": max(m for _, m, _ in self.samples) if self.samples else None,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml, 1 ms"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -169,7 +229,7 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 # ----------------------------------------------------------------------------- the path
@@ -456,9 +516,9 @@ def run_mxg(args, wl, ws_world, rank, local):
     # ---- timed region: K steps, per-step and per-kernel CUDA events
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in stages] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    clocks = ClockSampler(local, str(uuid) if uuid is not None else None)
     clocks.start()
-    time.sleep(0.3)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -658,7 +718,7 @@ def run_reference(args, wl, ws_world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mxg", choices=["mxg", "reference"])
     ap.add_argument("--config", default="mixtral_fprop_mxfp8")
