@@ -513,6 +513,28 @@ def run_mxg(args, wl, ws_world, rank, local):
     if int(path.status.item()) != 0:
         raise RuntimeError("device status %d after warm-up" % int(path.status.item()))
 
+    # one CUDA graph per stage, captured after the warm-up: the timed steps
+    # replay them with CUDA events around each replay on this stream
+    graphs, graph_note, graph_launches = None, None, 0
+    if not args.no_graph:
+        try:
+            n0 = mxg.mxg_launch_count()
+            graphs = []
+            for _, fn in stages:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                graphs.append(g)
+            graph_launches = mxg.mxg_launch_count() - n0  # kernels one replay of all stages runs
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+            if int(path.status.item()) != 0:
+                raise RuntimeError("device status %d after graph replay" % int(path.status.item()))
+        except Exception as e:  # capture unavailable: time eager launches instead
+            graphs, graph_note = None, "graph capture failed (%s); eager launches timed" % e
+            torch.cuda.synchronize()
+
     # ---- timed region: K steps, per-step and per-kernel CUDA events
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in stages] for _ in range(args.steps)]
@@ -526,15 +548,20 @@ def run_mxg(args, wl, ws_world, rank, local):
     t_wall = time.perf_counter()
     for s in range(args.steps):
         flush.fill_(1.0)
-        for (name, fn), (e0, e1) in zip(stages, ev[s]):
+        for i, ((name, fn), (e0, e1)) in enumerate(zip(stages, ev[s])):
             e0.record(stream)
-            fn()
+            if graphs is not None:
+                graphs[i].replay()
+            else:
+                fn()
             e1.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
-    launches = mxg.mxg_launch_count() - launches0
+    # graph replays do not pass through the C ABI: count what one capture launched
+    launches = (graph_launches * args.steps if graphs is not None
+                else mxg.mxg_launch_count() - launches0)
     clk = clocks.stop()
     per_kernel = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
                   for i, (name, _) in enumerate(stages)}
@@ -576,6 +603,9 @@ def run_mxg(args, wl, ws_world, rank, local):
                    "mode": wl.mode, "out": args.out, "epilogue": args.epilogue,
                    "step": " -> ".join(n for n, _ in stages),
                    "l2": "flushed before every timed step (512 MB write); inputs also exceed L2",
+                   "timing": graph_note or ("CUDA events around CUDA-graph replays (one graph per "
+                                            "kernel)" if graphs is not None else
+                                            "CUDA events around eager launches"),
                    "parallelism": "replicas" if ws_world > 1 else "single GPU"},
         "roofline": roofline,
         "kernels": kernels,
@@ -728,6 +758,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--M", type=int, default=0, help="override live rows (profiling runs)")
     ap.add_argument("--N", type=int, default=0, help="override N (profiling runs)")
     ap.add_argument("--K", type=int, default=0, help="override K (profiling runs)")
