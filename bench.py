@@ -567,6 +567,7 @@ def run_mxg(args, wl, ws_world, rank, local):
                   for i, (name, _) in enumerate(stages)}
     step_ms = [ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]
     ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
+    ms_median = max_over_ranks(float(np.median(step_ms)), dist, dev)
     if int(path.status.item()) != 0:
         raise RuntimeError("device status %d" % int(path.status.item()))
 
@@ -596,6 +597,7 @@ def run_mxg(args, wl, ws_world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "ms_per_step_median": round(ms_median, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4(e2m1/ue4m3)->f32" if nvfp4 else "mxfp8(e4m3/e8m0)->f32",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
