@@ -236,13 +236,14 @@ class ClockSampler:
 class Path:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, wl, out_bf16: bool, dev, rank: int = 0, epilogue: str = "none"):
+    def __init__(self, wl, out_bf16: bool, dev, rank: int = 0, epilogue: str = "none",
+                 inputs=None):
         import torch
         from moe_grouped_block_gb300 import mxg, workloads
         self.mxg, self.torch = mxg, torch
         self.wl = wl
         self.dev = dev
-        inp = workloads.make_inputs(replica_workload(wl, rank))
+        inp = inputs if inputs is not None else workloads.make_inputs(replica_workload(wl, rank))
         self.host = inp
         G, N, K, R = wl.G, wl.N, wl.K, wl.rows_capacity
         self.G, self.N, self.K, self.R = G, N, K, R
@@ -459,6 +460,65 @@ def measure_e2e(path, step, args, dist, dev, flush, stream):
     return ms, h2d, d2h
 
 
+def measure_e2e_pipelined(paths, args, dist, dev):
+    """End to end with host buffers, two buffer sets in flight: every step
+    copies its inputs from pinned host memory (copy stream), runs the C-ABI
+    calls (compute stream) and copies its output back (a third stream); step
+    i + 1's input copies overlap step i's compute and output copy, which run
+    on the other direction of the link.  Returns ms per step in steady state
+    (K steps between a start event before the first copy and an end event
+    after the last output copy)."""
+    import torch
+    host_in = [(n, t.cpu().pin_memory()) for n, t in paths[0].input_tensors()]
+    host_out = [torch.empty(p.C.shape, dtype=p.C.dtype).pin_memory() for p in paths]
+    dev_in = [dict(p.input_tensors()) for p in paths]
+    stages = [p.stages() for p in paths]
+    sh, sc, sd = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in paths]
+    ev_comp = [torch.cuda.Event() for _ in paths]
+    ev_out = [torch.cuda.Event() for _ in paths]
+
+    def issue(i):
+        b = i % 2
+        if i >= 2:
+            sh.wait_event(ev_comp[b])  # set b's inputs are no longer read
+        with torch.cuda.stream(sh):
+            for n, t in host_in:
+                dev_in[b][n].copy_(t, non_blocking=True)
+            ev_in[b].record(sh)
+        sc.wait_event(ev_in[b])
+        if i >= 2:
+            sc.wait_event(ev_out[b])  # set b's output has been copied out
+        with torch.cuda.stream(sc):
+            for _, fn in stages[b]:
+                fn()
+            ev_comp[b].record(sc)
+        sd.wait_event(ev_comp[b])
+        with torch.cuda.stream(sd):
+            host_out[b].copy_(paths[b].C, non_blocking=True)
+            ev_out[b].record(sd)
+
+    for i in range(2):
+        issue(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(sh)
+    for i in range(args.steps):
+        issue(i)
+    t1.record(sd)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dist, dev)
+    # both buffer sets computed the same step: their outputs agree bit for bit
+    if not torch.equal(host_out[0], host_out[1]):
+        raise RuntimeError("the two e2e buffer sets disagree")
+    for p in paths:
+        if int(p.status.item()) != 0:
+            raise RuntimeError("device status %d in the e2e run" % int(p.status.item()))
+    return ms
+
+
 def gemm_roofline(gemm_name, flops, gemm_bytes, gemm_ms, peaks, peak_src, nvfp4, traffic):
     """The roofline object of the GEMM launch.  Its roofline time is the larger
     of its algorithmic FLOP at the dense tensor peak (measured bf16 x 2 for
@@ -574,6 +634,15 @@ def run_mxg(args, wl, ws_world, rank, local):
     # ---- e2e: host buffers, copies inside the timed region
     e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else measure_e2e(path, step, args, dist, dev,
                                                                       flush, stream)
+    e2e_pipe_ms = None
+    if not args.no_e2e:
+        path2 = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue,
+                     inputs=path.host)
+        if path.bias is not None:  # the same epilogue operands in both sets
+            path2.bias.copy_(path.bias)
+            path2.alpha.copy_(path.alpha)
+        e2e_pipe_ms = measure_e2e_pipelined([path, path2], args, dist, dev)
+        del path2
 
     peaks, peak_src = load_peaks()
     flops = wl.flops()
@@ -612,10 +681,16 @@ def run_mxg(args, wl, ws_world, rank, local):
         "roofline": roofline,
         "kernels": kernels,
         "e2e": None if e2e_ms is None else {
-            "value": round(job_tflops(flops, ws_world, e2e_ms), 2), "unit": "TFLOP/s",
-            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "same C-ABI calls; inputs copied from pinned host memory and the output copied "
-                    "back inside each timed step"},
+            "value": round(job_tflops(flops, ws_world, e2e_pipe_ms), 2), "unit": "TFLOP/s",
+            "ms_per_step": round(e2e_pipe_ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "same C-ABI calls; every step copies its inputs from pinned host memory and its "
+                    "output back inside the timed region, with two buffer sets so that step i+1's "
+                    "input copies overlap step i's compute and output copy (steady state over K "
+                    "steps)",
+            "serial": {"value": round(job_tflops(flops, ws_world, e2e_ms), 2),
+                       "ms_per_step": round(e2e_ms, 4),
+                       "note": "copy in, compute, copy out, one step at a time"}},
         "gpu_launches": int(launches),
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 4),
