@@ -1,7 +1,8 @@
 """Host logic of the benchmark's GEMM roofline object (no GPU): the bound is
 whichever roofline time is larger, FLOP at the dense tensor peak or
 algorithmic bytes at the measured HBM bandwidth, and frac is the achieved
-fraction of that peak, equal to t_roofline / t."""
+fraction of that peak, equal to t_roofline / t; the measured DRAM traffic is
+reported only while the GEMM sources hash to the digest it was taken on."""
 import os
 import sys
 
@@ -50,3 +51,34 @@ def test_finegrained_sits_just_on_the_tensor_side():
     r = bench.gemm_roofline("g", flops, nbytes, 0.0924, PEAKS, "measured", False, None)
     assert r["bound"] == "tensor"
     assert r["t_tensor_roofline_ms"] > r["t_hbm_roofline_ms"]
+
+
+ROW = "| mixtral_fprop_mxfp8 | `k` | 568991744 | 446700800 | 1015692544 | 620.7 | alg |\n"
+
+
+def test_traffic_is_reported_only_for_the_measured_sources(tmp_path, monkeypatch):
+    head = "| workload | kernel | read bytes | write bytes | traffic bytes | us | alg |\n|---|---|---|---|---|---|---|\n"
+    fresh = tmp_path / "fresh.md"
+    fresh.write_text("sources sha256: `%s`\n\n" % bench.gemm_source_digest() + head + ROW)
+    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(fresh))
+    assert bench.measured_traffic("mixtral_fprop_mxfp8") == 1015692544
+    assert bench.measured_traffic("no_such_workload") is None
+    # the same table measured on other sources (the kernel changed since): none
+    stale = tmp_path / "stale.md"
+    stale.write_text("sources sha256: `%s`\n\n" % ("0" * 64) + head + ROW)
+    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(stale))
+    assert bench.measured_traffic("mixtral_fprop_mxfp8") is None
+    # no summary at all: none
+    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(tmp_path / "absent.md"))
+    assert bench.measured_traffic("mixtral_fprop_mxfp8") is None
+
+
+def test_traffic_table_row_is_read_by_workload(tmp_path, monkeypatch):
+    digest = bench.gemm_source_digest()
+    table = ("sources sha256: `%s`\n\n| workload | kernel | read bytes | write bytes | traffic bytes |\n"
+             "|---|---|---|---|---|\n| wl_a | `k` | 1 | 2 | 3 |\n| wl_b | `k` | 10 | 20 | 30 |\n" % digest)
+    f = tmp_path / "traffic.md"
+    f.write_text(table)
+    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(f))
+    assert bench.measured_traffic("wl_a") == 3
+    assert bench.measured_traffic("wl_b") == 30
