@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256, 3)
     mxfp8_quantize_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                           const int64_t* __restrict__ group_ws, int G, uint8_t* __restrict__ q_row,
                           uint8_t* __restrict__ sf_row, uint8_t* __restrict__ q_col,
-                          uint8_t* __restrict__ sf_col, int qcol_v8, int64_t cap_col,
+                          uint8_t* __restrict__ sf_col, int qcol_v8, int qrow_v8, int64_t cap_col,
                           int32_t* status) {
   extern __shared__ uint8_t qsmem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) &
@@ -223,20 +223,22 @@ __global__ void __launch_bounds__(256, 3)
     return r;
   };
 
-  // thread 0 issues the TMA load of tile t into buffer b
+  // thread 0 issues the TMA loads of tile t into buffer b: two 64-column
+  // boxes (128 rows x 128 bytes each, 128-byte swizzle: 16-byte chunk c of row
+  // r sits at chunk position c ^ (r & 7))
   auto issue = [&](int64_t t, int b) {
     const uint32_t bar = smem_u32(&bars[b]);
+    const int32_t x0 = static_cast<int32_t>((t % kt) << 7);
+    const int32_t y = static_cast<int32_t>(row_tile(t / kt).m0);
     mbar_arrive_expect_tx(bar, kQTileBytes);
-    tma_load_2d(smem_u32(sm + b * kQTileBytes), &tmap_x, bar, static_cast<int32_t>((t % kt) << 7),
-                static_cast<int32_t>(row_tile(t / kt).m0));
+    tma_load_2d(smem_u32(sm + b * kQTileBytes), &tmap_x, bar, x0, y);
+    tma_load_2d(smem_u32(sm + b * kQTileBytes + kQTileBytes / 2), &tmap_x, bar, x0 + 64, y);
   };
   if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
     prefetch_tmap(&tmap_x);
     issue(blockIdx.x, 0);
   }
 
-  const uint32_t half = lane >> 4;  // which row of the pair
-  const uint32_t cl = lane & 15u;   // 16-byte chunk: columns 8*cl .. 8*cl+7
   uint32_t parity = 0u;  // bit b: phase parity of buffer b
   uint32_t pending = static_cast<int64_t>(blockIdx.x) < tiles ? 1u : 0u;  // thread 0's loads
   int b = 0;
@@ -262,29 +264,51 @@ __global__ void __launch_bounds__(256, 3)
       // rows past the group: zeros (their scales come out 0, their colwise
       // bytes are the padding); ordered before the buffer's next TMA write
       uint32_t* wt = reinterpret_cast<uint32_t*>(sm + b * kQTileBytes);
-      for (int w = rtl.valid * 64 + static_cast<int>(threadIdx.x); w < 128 * 64; w += 256) wt[w] = 0;
+      for (int w = static_cast<int>(threadIdx.x); w < 128 * 64; w += 256)
+        if (((w & 4095) >> 5) >= rtl.valid) wt[w] = 0;  // word w: box w >> 12, row (w >> 5) & 127
       fence_proxy_async_shared();
       __syncthreads();
     }
 
-    // ---- phase 1: rows (16 lanes per row, 16-byte chunks; conflict-free per 8-lane phase)
+    // ---- phase 1: rows.  A lane owns one 32-element block (row r, block blk):
+    // four 16-byte loads, its own amax and scale, one 32-byte store.  The 8
+    // lanes of each 8-lane phase read 8 rows of one block: 8 different chunk
+    // positions under the swizzle, so the loads are conflict-free.
     if (ROW) {
       uint8_t* sfr = sf_row + ((mp >> 7) * kt + (k0 >> 7)) * 512;  // this tile's scale tile
-#pragma unroll 4
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t r = i * 16 + warp * 2 + half;
-        const uint4 v = reinterpret_cast<const uint4*>(tile)[r * 16 + cl];
-        const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(v.x, v.y), bf16x2_max_abs(v.z, v.w));
-        float a = fmaxf(abs_lo(m), abs_hi(m));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        const int e = mx_exponent(a);
-        const uint32_t sb = bf16_pow2_neg_bits(e);
-        const uint2 o = quant8(v, sb | (sb << 16));
-        if (!UNA || static_cast<int>(r) < rtl.valid)
-          *reinterpret_cast<uint2*>(q_row + (m0 + r) * cols + k0 + 8 * cl) = o;
-        if ((cl & 3u) == 0)
-          sfr[(r & 31u) * 16 + (r >> 5) * 4 + (cl >> 2)] = static_cast<uint8_t>(e + 127);
+      const uint32_t rl = lane & 7u, blk = lane >> 3;
+      const uint4* box = reinterpret_cast<const uint4*>(tile + (blk >> 1) * 4096);
+      const uint32_t c0 = (blk & 1u) * 4u;  // the block's first chunk in its 128-byte row
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t r = static_cast<uint32_t>(i) * 64u + warp * 8u + rl;
+        uint4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = box[r * 8 + ((c0 + q) ^ (r & 7u))];
+        uint32_t m = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(v[q].x, v[q].y),
+                                               bf16x2_max_abs(v[q].z, v[q].w)));
+        const int e = mx_exponent(fmaxf(abs_lo(m), abs_hi(m)));
+        const uint32_t sb = bf16_pow2_neg_bits(e), s2 = sb | (sb << 16);
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint2 h = quant8(v[q], s2);
+          o[2 * q] = h.x;
+          o[2 * q + 1] = h.y;
+        }
+        if (!UNA || static_cast<int>(r) < rtl.valid) {
+          uint8_t* dst = q_row + (m0 + r) * cols + k0 + 32 * blk;
+          if (qrow_v8) {
+            st_global_32B(dst, o);
+          } else {
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        sfr[(r & 31u) * 16 + (r >> 5) * 4 + blk] = static_cast<uint8_t>(e + 127);
       }
     }
 
@@ -295,19 +319,25 @@ __global__ void __launch_bounds__(256, 3)
       // pass A: block amax of both columns at once (packed); pass B: re-read,
       // scale both halves by their own power of two and convert.  A warp reads
       // 32 consecutive words per row: no bank conflicts.
-      const uint32_t* col = tile + (32 * j) * 64 + cp;
+      // word (row 32j + i, pair cp) of the swizzled tile: box cp >> 5, chunk
+      // ((cp & 31) >> 2) ^ (i & 7), word cp & 3 of the chunk (32 words a row)
+      const uint32_t* col = tile + (cp >> 5) * 4096 + (32 * j) * 32;
+      uint32_t off[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) off[k] = ((((cp & 31u) >> 2) ^ static_cast<uint32_t>(k)) << 2) | (cp & 3u);
+      auto word = [&](int i) { return col[i * 32 + off[i & 7]]; };
       uint32_t m = 0;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) m = bf16x2_max_abs(m, col[i * 64]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = bf16x2_max_abs(m, word(i));
       const int elo = mx_exponent(abs_lo(m)), ehi = mx_exponent(abs_hi(m));
       const uint32_t s2 = bf16_pow2_neg_bits(elo) | (bf16_pow2_neg_bits(ehi) << 16);
       uint32_t olo[8], ohi[8];  // 32 E4M3 bytes of column 2cp / 2cp+1
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t u0 = bf16x2_mul(col[(4 * i) * 64], s2);
-        const uint32_t u1 = bf16x2_mul(col[(4 * i + 1) * 64], s2);
-        const uint32_t u2 = bf16x2_mul(col[(4 * i + 2) * 64], s2);
-        const uint32_t u3 = bf16x2_mul(col[(4 * i + 3) * 64], s2);
+        const uint32_t u0 = bf16x2_mul(word(4 * i), s2);
+        const uint32_t u1 = bf16x2_mul(word(4 * i + 1), s2);
+        const uint32_t u2 = bf16x2_mul(word(4 * i + 2), s2);
+        const uint32_t u3 = bf16x2_mul(word(4 * i + 3), s2);
         olo[i] = cvt_e4m3x2(bf16lo(u0), bf16lo(u1)) | (cvt_e4m3x2(bf16lo(u2), bf16lo(u3)) << 16);
         ohi[i] = cvt_e4m3x2(bf16hi(u0), bf16hi(u1)) | (cvt_e4m3x2(bf16hi(u2), bf16hi(u3)) << 16);
       }
@@ -349,8 +379,8 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
   if (max_tiles == 0) return cudaSuccess;
   CUtensorMap tm;
   if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, static_cast<uint64_t>(cols),
-                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 128, 128,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
+                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 64, 128,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const int smem = kQSmemBytes + (unaligned ? 12 * (G + 1) + 16 : 0);
   auto launch = [&](auto kern) {
@@ -364,8 +394,9 @@ cudaError_t launch_mxfp8_quantize(bool row, bool col, const uint16_t* x, int64_t
     const int64_t full = static_cast<int64_t>(num_sms) * per_sm;
     const int grid = static_cast<int>(max_tiles < full ? max_tiles : full);
     const int qcol_v8 = (reinterpret_cast<uintptr_t>(q_col) & 31u) == 0 ? 1 : 0;
+    const int qrow_v8 = (reinterpret_cast<uintptr_t>(q_row) & 31u) == 0 ? 1 : 0;
     kern<<<grid, 256, smem, stream>>>(tm, cap, cols, group_ws, G, q_row, sf_row, q_col, sf_col,
-                                       qcol_v8, cap_col, status);
+                                       qcol_v8, qrow_v8, cap_col, status);
     return cudaGetLastError();
   };
   if (unaligned) {
