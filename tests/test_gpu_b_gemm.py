@@ -366,3 +366,37 @@ def test_nvfp4_wgrad_scaled(K):
             assert not got[g].any()
         else:
             assert np.abs(got[g] - ref[g]).max() / np.abs(ref[g]).max() <= TOL, g
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_empty_routing_fprop_is_a_noop_and_wgrad_zero_fills(tn):
+    """Every group empty (M = 0 live rows): fprop writes nothing, wgrad writes
+    dW_g = 0 for every group (no beta), and no status bit is set."""
+    G, N, K, R = 4, 256, 512, 1024
+    zero = torch.zeros(G, dtype=torch.int32)
+    x = workloads.random_bf16((R, K), seed=41).to(DEV)
+    w = workloads.random_bf16((G * N, K), seed=42, scale=0.02).to(DEV)
+    dy = workloads.random_bf16((R, N), seed=43, scale=1e-3).to(DEV)
+    # fprop
+    ws, st = gpu_offsets(zero, K, R)
+    qx, _ = gpu_mxfp8(x, ws, G, mxg.MXG_ROWWISE)
+    qw, _ = gpu_mxfp8(w, None, G, mxg.MXG_ROWWISE)
+    C = torch.full((R, N), 5.0, dtype=torch.float32, device=DEV)
+    with tile_n(tn):
+        mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, (qx["q_row"], qx["sf_row"], None),
+                             (qw["q_row"], qw["sf_row"], None), ws, G, R, N, K, C=C, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.all(C == 5.0), "fprop wrote rows with no live group"
+    # wgrad
+    ws2, st2 = gpu_offsets(zero, K, R)
+    qxc, _ = gpu_mxfp8(x, ws2, G, mxg.MXG_COLWISE)
+    qdc, _ = gpu_mxfp8(dy, ws2, G, mxg.MXG_COLWISE)
+    dW = torch.full((G, N, K), 3.0, dtype=torch.float32, device=DEV)
+    with tile_n(tn):
+        mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_WGRAD_NT, (qdc["q_col"], qdc["sf_col"], None),
+                             (qxc["q_col"], qxc["sf_col"], None), ws2, G, R, N, K, None, None, dW,
+                             dev_status=st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert torch.all(dW == 0.0), "wgrad must zero-fill every dW_g of an empty group"
