@@ -55,14 +55,24 @@ GEMM_SOURCES = ("gemm.cu", "mxg_device.cuh", "mxg_host.h", "tmap.cu")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "grouped_gemm_pair_kernel_dram_traffic.md")
 
 
+def code_only(text: str) -> str:
+    """C/C++ source without its comments and with runs of whitespace folded, so
+    that an edit of comments alone leaves the digest below unchanged."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def gemm_source_digest() -> str:
-    """sha256 over the GEMM kernel's sources, in a fixed order: a DRAM traffic
-    figure is reported only while the kernel it was measured on is unchanged."""
+    """sha256 over the GEMM kernel's sources (code only, in a fixed order): a
+    DRAM traffic figure is reported only while the kernel it was measured on is
+    unchanged."""
     import hashlib
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "moe_grouped_block_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "moe_grouped_block_gb300", "csrc", f)) as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()
 
 

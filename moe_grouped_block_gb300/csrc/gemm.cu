@@ -14,14 +14,20 @@
 // scaling is fused into the read-out).
 //
 // Design (GB300-first, no library):
-//   * one CTA per SM, persistent; tiles are walked in a static round-robin
-//     order derived on the device from the offsets workspace, so there is no
-//     host sync and the launch is graph-safe (PR #2763's motivation).
-//   * warp 0 lane 0: TMA producer (A and B tiles with the 128-byte swizzle,
-//     scale tiles as plain bulk copies); warp 1 lane 0: MMA issuer;
-//     warps 2..: epilogue, one TMEM lane quarter and 128 columns each.
-//   * tile 128 x BN, 128 bytes of K per pipeline stage = 4 MMAs of 32 bytes
-//     (32 E4M3 or 64 E2M1 elements each).
+//   * one CTA per SM, persistent; work units are walked in a static
+//     round-robin order derived on the device from the offsets workspace, so
+//     there is no host sync and the launch is graph-safe (PR #2763's
+//     motivation).
+//   * default: grouped_gemm_pair_kernel, 2-CTA clusters computing 256 x 256
+//     units with the cta_group::2 MMA (each CTA holds 128 rows of A and half
+//     of B); warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer (even CTA),
+//     warps 2-9 epilogue (one TMEM lane quarter and 128 columns each), warps
+//     10-11 scale copies (even CTA).  128 bytes of K per pipeline stage (4
+//     MMAs of 32 bytes: 32 E4M3 or 64 E2M1 elements), 256 bytes for MXFP8
+//     fprop when K % 256 == 0, 64 for NVFP4 where 256 elements do not fit.
+//   * grouped_gemm_kernel: single-CTA 128 x BN tiles (BN 256 or 128) for the
+//     cases the pair does not cover (B with fewer than 256 rows) and the
+//     tile-width experiments; warps 0 / 1 / 2.. as above, copies inline.
 //   * scales: each 128x4 swizzled scale tile (512 bytes) is copied into 4
 //     TMEM columns by tcgen05.cp 32x128b.warpx4 -- the swizzled layout is
 //     exactly the one that copy and the block-scaled MMA consume.  Each

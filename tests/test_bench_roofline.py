@@ -82,3 +82,11 @@ def test_traffic_table_row_is_read_by_workload(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(f))
     assert bench.measured_traffic("wl_a") == 3
     assert bench.measured_traffic("wl_b") == 30
+
+
+def test_digest_ignores_comments_but_not_code():
+    src = "int f(int a) {  // returns a + 1\n  /* block\n comment */ return a + 1;\n}\n"
+    same = "int f(int a) {\n  return a + 1;   // reworded comment\n}\n"
+    other = "int f(int a) {\n  return a + 2;\n}\n"
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(other)
