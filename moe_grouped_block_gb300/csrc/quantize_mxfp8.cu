@@ -11,21 +11,21 @@
 //
 // Work unit: a 128-row x 128-column tile of bf16 (32 KB read).  Its rowwise
 // scales are exactly one 512-byte swizzle tile of sf_row, and its colwise
-// scales exactly one 512-byte tile of sf_col, so both are staged in shared
-// memory and written as 16-byte stores.
-//   load:    one thread issues a TMA copy of the CTA's next tile into the
-//            second of two shared-memory buffers while all threads work on
-//            the current one, so a tile's HBM latency overlaps the previous
-//            tile's arithmetic and stores.
-//   phase 1: each half-warp reads one row segment (16 lanes x 16 bytes,
-//            conflict-free per 8-lane phase), a 4-lane shuffle gives the 1x32
-//            block amax, and the E4M3 bytes go straight out (8 bytes per
-//            lane, 128 contiguous per row).
+// scales exactly one 512-byte tile of sf_col; each thread writes its scale
+// bytes straight to their swizzled places.
+//   load:    one thread issues the TMA copies (two 64-column boxes with the
+//            128-byte swizzle) of the CTA's next tile into the second of two
+//            shared-memory buffers while all threads work on the current one,
+//            so a tile's HBM latency overlaps the previous tile's arithmetic
+//            and stores; one __syncthreads per tile.
+//   phase 1: a lane owns one 1x32 block: four 16-byte loads (the 8 lanes of a
+//            load phase read 8 rows of one block, 8 distinct swizzled chunk
+//            positions: conflict-free), its amax and scale, one 32-byte store.
 //   phase 2: thread (column pair, 32-row block) walks 32 words down the tile
-//            twice (a warp reads 32 consecutive words per row: no bank
-//            conflicts) -- once for the 32x1 block amax of both columns, once
-//            to quantize -- and writes 32 contiguous bytes of each transposed
-//            row.
+//            twice through precomputed swizzled offsets (a warp reads 32
+//            distinct chunk words per row: no bank conflicts) -- once for the
+//            32x1 block amax of both columns, once to quantize -- and writes
+//            32 contiguous bytes of each transposed row.
 //   arithmetic: amax and the scaling by 2^-e run on packed bf16 pairs.  The
 //            maximum of magnitudes is exact; so is the product by a power of
 //            two whenever it is a normal bf16 (|x| 2^-e <= 448 bounds it
