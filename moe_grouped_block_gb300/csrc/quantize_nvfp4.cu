@@ -11,11 +11,17 @@
 // Operations are explicit __fdiv_rn / __fmul_rn so the compiler cannot fuse
 // or reassociate them.
 //
-// One warp per row: pass 1 reads the row (32 lanes x 16 bytes per step) for
-// the row amax; pass 2 reads it again (from L1/L2) one 16-element block per
-// lane, writes 8 packed bytes per lane (256 contiguous bytes per warp step)
-// and gathers each run of 4 scale bytes -- which are contiguous in the
-// swizzled layout -- into one 32-bit store.
+// Rowwise: rows of up to 7168 columns go through shared memory -- one lane
+// brings a whole row in with one bulk copy and a pair of warps works it (the
+// row amax, then one 16-element block per lane: 8 packed bytes per lane and
+// each run of 4 scale bytes, contiguous in the swizzled layout, as one 32-bit
+// store); wider rows take one warp per row that reads the row twice from
+// global memory.
+// Colwise (the wgrad operands, per-(group, column) outer scale): zero the
+// [G, cols] outer buffer; an amax pass over 128 x 128 TMA-staged tiles folds
+// column maxima into it with atomicMax; a quantize pass walks the tiles in
+// reverse order (starting on the tiles still in L2) and writes the transposed
+// codes and swizzled scales; a last launch turns the amax into A / 2688.
 #include <algorithm>
 
 #include "mxg_device.cuh"
