@@ -2,7 +2,8 @@
 whichever roofline time is larger, FLOP at the dense tensor peak or
 algorithmic bytes at the measured HBM bandwidth, and frac is the achieved
 fraction of that peak, equal to t_roofline / t; the measured DRAM traffic is
-reported only while the GEMM sources hash to the digest it was taken on."""
+reported only while the GEMM sources hash to the digest it was taken on; the
+clock record's throttle reasons are read from nvidia-smi lines or NVML bits."""
 import os
 import sys
 
@@ -90,3 +91,41 @@ def test_digest_ignores_comments_but_not_code():
     other = "int f(int a) {\n  return a + 2;\n}\n"
     assert bench.code_only(src) == bench.code_only(same)
     assert bench.code_only(src) != bench.code_only(other)
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+    def kill(self):
+        pass
+
+
+class _Joined:
+    def join(self, timeout=None):
+        pass
+
+
+def test_clock_reasons_from_nvidia_smi_lines():
+    c = bench.ClockSampler(0)
+    c.proc, c.t = _Done(), _Joined()
+    c.lines = ["2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+               "1980, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+               "2070, 2070, 1200.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active",
+               "garbage line"]
+    r = c.stop()
+    assert r["sm_mhz"] == 2070 and r["sm_max_mhz"] == 2070 and r["samples"] == 3
+    assert r["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_clock_reasons_from_nvml_samples():
+    c = bench.ClockSampler(0)
+    c.nvml, c.t, c.running = object(), _Joined(), True
+    c.samples = [(2070, 2070, 0x0), (2070, 2070, 0x4), (1500, 2070, 0x40), (2070, 2070, 0x1)]
+    r = c.stop()
+    assert r["sm_mhz"] == 2070 and r["sm_max_mhz"] == 2070 and r["samples"] == 4
+    # 0x1 (idle) is not a throttle reason; 0x4 power cap, 0x40 hardware thermal
+    assert r["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
