@@ -115,8 +115,11 @@ size_t mxg_offsets_workspace_bytes(int G);
  * Sanitisation (recorded in dev_status): a negative size counts as 0
  * (NEG_SIZE); a size not a multiple of 128 is rounded down (MISALIGNED);
  * rows past rows_capacity are dropped (SUM_OVER_CAPACITY).
+ * A size times the multiplier is formed exactly (no 64-bit overflow): a
+ * product past rows_capacity is clamped to it.
  * Errors: MXG_ERR_INVALID_ARG for null sizes/ws, G < 1 or G > 65536,
- * multiplier < 1, last_dim < 1 or rows_capacity < 0. */
+ * multiplier < 1 or > 2^31, last_dim < 1, rows_capacity < 0 or > 2^62, or
+ * rows_capacity * last_dim beyond int64. */
 mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int64_t multiplier,
                                int64_t last_dim, int64_t rows_capacity, int64_t* ws,
                                int32_t* dev_status, mxg_stream_t stream);
@@ -223,22 +226,33 @@ mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_
                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
                               mxg_stream_t stream);
 
-/* Test hook for the failure path of the GEMM's bounded pipeline waits (no
- * counterpart on the pages).  Same arguments and checks as mxg_grouped_gemm,
- * plus:
+/* Test entry point (no counterpart on the pages): mxg_grouped_gemm with the
+ * kernel choices that the parity tests need to reach every variant, and a
+ * hook for the failure path of the bounded pipeline waits.  Same arguments
+ * and checks as mxg_grouped_gemm, plus:
+ *   tile_n          : 0 -- the default kernel choice (the CTA-pair kernel
+ *                     with 256 x 256 units when B has at least 256 rows);
+ *                     256 or 128 -- the single-CTA kernel with 128 x 256 or
+ *                     128 x 128 tiles (256 only where the output width is a
+ *                     multiple of 256, else 128).
+ *   stage_bytes     : 0 -- default; 128 -- 128 bytes of K per pipeline stage
+ *                     where the default takes 256 (MXFP8 fprop, K % 256 == 0).
  *   inject_flags    : bit 0 -- CTA 0 withholds the arrival that tells its
  *                     epilogue that its first accumulator is ready, so the
  *                     epilogue's wait runs out; 0 -- a normal run.
  *   wait_timeout_ns : bound on every pipeline wait, in ns (0 = 1 s default).
  * With bit 0 set the launch ends with MXG_DEV_TIMEOUT in dev_status, the
  * affected CTA drains its copies and MMAs, frees its tensor memory and
- * returns; the output is undefined and the device stays usable. */
+ * returns; the output is undefined and the device stays usable.
+ * Errors: as mxg_grouped_gemm, plus INVALID_ARG for another tile_n or
+ * stage_bytes value or unknown inject bits. */
 mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
                                     const mxg_operand_t* B, const int64_t* group_ws, int G,
                                     int64_t M_cap, int64_t N, int64_t K, const float* alpha,
                                     const float* beta, const float* bias, void* C,
-                                    mxg_out_t out_type, int32_t* dev_status, int inject_flags,
-                                    int64_t wait_timeout_ns, mxg_stream_t stream);
+                                    mxg_out_t out_type, int32_t* dev_status, int tile_n,
+                                    int stage_bytes, int inject_flags, int64_t wait_timeout_ns,
+                                    mxg_stream_t stream);
 
 /* Workspace bytes mxg_grouped_gemm needs (0 for every combination here). */
 size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,
@@ -284,8 +298,9 @@ mxg_status_t mxg_group_offsets_unaligned(const void* sizes, int sizes_is_int64, 
  * rows, with the block rules of mxg_group_quantize.  Rows and columns past
  * the padded groups are not written.  Unused output pointers may be NULL.
  * Errors: INVALID_ARG (null x or group_ws, G < 1 or G > 1024, bad layout,
- * null required output), ALIGNMENT (rows_capacity or cols not multiples of
- * 128, pointers not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
+ * null required output, rows_capacity + 128 * G above 2^31 - 128),
+ * ALIGNMENT (rows_capacity or cols not multiples of 128, pointers not
+ * 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
 mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
                                           int64_t rows_capacity, int64_t cols,
                                           const int64_t* group_ws, int G, uint8_t* q_row,
@@ -303,7 +318,7 @@ mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
  *   DGRAD_NN : A data [M_cap, N] dense, A scale [R_pad, N/32] padded.
  * Output rows are the dense data rows; rows past a group are not written.
  * Errors: as mxg_grouped_gemm, plus INVALID_ARG when B has fewer than 256
- * rows (G * N for fprop, K otherwise). */
+ * rows (G * N for fprop, K otherwise) or M_cap + 128 * G exceeds 2^31 - 128. */
 mxg_status_t mxg_grouped_gemm_unaligned(mxg_gemm_mode_t mode, const mxg_operand_t* A,
                                         const mxg_operand_t* B, const int64_t* group_ws, int G,
                                         int64_t M_cap, int64_t N, int64_t K, const float* alpha,

@@ -26,8 +26,8 @@
 //     MMAs of 32 bytes: 32 E4M3 or 64 E2M1 elements), 256 bytes for MXFP8
 //     fprop when K % 256 == 0, 64 for NVFP4 where 256 elements do not fit.
 //   * grouped_gemm_kernel: single-CTA 128 x BN tiles (BN 256 or 128) for the
-//     cases the pair does not cover (B with fewer than 256 rows) and the
-//     tile-width experiments; warps 0 / 1 / 2.. as above, copies inline.
+//     cases the pair does not cover (B with fewer than 256 rows); warps
+//     0 / 1 / 2.. as above, scale copies inline on the MMA thread.
 //   * scales: each 128x4 swizzled scale tile (512 bytes) is copied into 4
 //     TMEM columns by tcgen05.cp 32x128b.warpx4 -- the swizzled layout is
 //     exactly the one that copy and the block-scaled MMA consume.  Each
@@ -63,15 +63,16 @@ struct GemmParams {
   int mode;  // 0 fprop, 1 wgrad, 2 dgrad
   int out_bf16;
   int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
-  int prefetch;  // L2 prefetch distance in K blocks (0 = off)
   int c_align32;  // C is 32-byte aligned (whole-sector epilogue stores)
   int unaligned;  // group sizes of any value (MXFP8, CTA-pair kernel only)
 };
 
 // BK: bytes of K per pipeline stage (128 with the 128-byte swizzle, or 64
-// with the 64-byte swizzle: half-size stages, twice as many of them).
+// with the 64-byte swizzle for row-scaled NVFP4: half-size stages, twice as
+// many of them).
 template <int BN, int STAGES, int ACC, bool NVF4, int BK = 128>
 struct GemmCfg {
+  static_assert(BK == 128 || (BK == 64 && NVF4), "64-byte stages are for NVFP4");
   static constexpr int kEpiWarps = 4 * (BN / 128);
   static constexpr int kThreads = 32 * (2 + kEpiWarps);
   static constexpr int kATile = 128 * BK;
@@ -80,7 +81,7 @@ struct GemmCfg {
   static constexpr int kSwizzle = BK == 128 ? 2 : 4;  // descriptor swizzle mode (128B / 64B)
   static constexpr int kSbo = 8 * BK;            // bytes between 8-row core-matrix groups
   // scale tiles along K per stage and band: NVFP4 one per MMA (64 elements);
-  // MXFP8 one 128-element tile, shared by two 64-byte stages when BK = 64
+  // MXFP8 one 128-element tile
   static constexpr int kAtomsK = NVF4 ? kMmas : 1;
   static constexpr int kSfaBytes = 512 * kAtomsK;
   static constexpr int kSfbBytes = 512 * kAtomsK * (BN / 128);
@@ -110,24 +111,19 @@ struct TileInfo {
   int g;
   int64_t a_row, b_row;      // first row of the A / B tile (TMA coordinate 1)
   int64_t a_sf_row;          // row of A's scales: the padded row when groups are unaligned
-  int64_t kb_count;          // K blocks (128 bytes) of this tile
+  int64_t kb_count;          // K blocks (BK bytes) of this tile
   int64_t a_kb0, b_kb0;      // first K block of A and of B
   int64_t c_row, c_col;      // top-left output element
   int64_t row_end;           // rows of C at or beyond this are not written
-  bool dup;                  // paired launch: this CTA's half of the pair is past the
-                             // group's last tile (it only helps load the shared B tile)
 };
 
-// Work unit t -> tile.  Unpaired: one 128 x BN output tile.  Paired (a
-// 2-CTA cluster): two vertically adjacent tiles sharing one B tile, CTA rank
-// r taking the (2u + r)-th row tile of the unit.
+// Work unit t of the single-CTA kernel -> one 128 x BN output tile.
 // K blocks are BK bytes: BK elements of E4M3, 2*BK of packed E2M1 (EPB =
 // elements per byte).
-template <int BN, bool PAIR, int BK, int EPB>
+template <int BN, int BK, int EPB>
 __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, const int32_t* row_off,
-                                             const int32_t* tile_off, uint32_t rank) {
+                                             const int32_t* tile_off) {
   TileInfo ti;
-  ti.dup = false;
   if (p.mode != 1) {  // fprop / dgrad: ragged output rows
     int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
     while (hi - lo > 1) {
@@ -138,15 +134,9 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
         hi = mid;
     }
     const int g = lo;
-    const int64_t mt = (row_off[g + 1] - row_off[g]) >> 7;
-    const int64_t mu = PAIR ? (mt + 1) >> 1 : mt;  // row units per column tile
+    const int64_t mt = (row_off[g + 1] - row_off[g]) >> 7;  // row tiles per column tile
     const int64_t local = t - tile_off[g];
-    const int64_t n_tile = local / mu, mu_i = local % mu;
-    int64_t m_tile = PAIR ? 2 * mu_i + rank : mu_i;
-    if (PAIR && m_tile >= mt) {
-      m_tile = 2 * mu_i;
-      ti.dup = true;
-    }
+    const int64_t n_tile = local / mt, m_tile = local % mt;
     ti.g = g;
     ti.a_row = row_off[g] + 128 * m_tile;
     // fprop: B rows are expert g's weight rows; dgrad: B is the transposed
@@ -159,16 +149,11 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.c_col = BN * n_tile;
     ti.row_end = row_off[g + 1];
   } else {
-    const int64_t nt = p.N >> 7, nu = PAIR ? (nt + 1) >> 1 : nt;
-    const int64_t kt = p.K / BN, tpg = nu * kt;
+    const int64_t nt = p.N >> 7;
+    const int64_t kt = p.K / BN, tpg = nt * kt;
     const int g = static_cast<int>(t / tpg);
     const int64_t local = t % tpg;
-    const int64_t nu_i = local / kt, k_tile = local % kt;
-    int64_t n_tile = PAIR ? 2 * nu_i + rank : nu_i;
-    if (PAIR && n_tile >= nt) {
-      n_tile = 2 * nu_i;
-      ti.dup = true;
-    }
+    const int64_t n_tile = local / kt, k_tile = local % kt;
     ti.g = g;
     ti.a_row = 128 * n_tile;
     ti.b_row = BN * k_tile;
@@ -342,14 +327,15 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
   }
 }
 
-// PAIR: launched as 2-CTA clusters; each CTA loads half of the shared B tile
-// and multicasts it to both, and each MMA issuer releases a stage in both
-// CTAs (a stage is refilled only once both CTAs' MMAs are done with it).
-template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR, int BK>
+// Single-CTA kernel: one 128 x BN output tile per work unit, ACC
+// accumulators in tensor memory (the MMA of the next tile starts while the
+// epilogue drains the previous one when ACC = 2).
+template <int BN, int STAGES, int ACC, bool NVF4, int BK>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
   using Cfg = GemmCfg<BN, STAGES, ACC, NVF4, BK>;
+  constexpr int EPB = NVF4 ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -372,7 +358,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIR ? 2 : 1);
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -386,18 +372,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     tmem_alloc(smem_u32(tmem_base_s), Cfg::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 1) build_group_tables(p, row_off, nullptr, tile_off, lane, PAIR, BN);
+  if (warp == 1) build_group_tables(p, row_off, nullptr, tile_off, lane, false, BN);
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // the partner's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_s;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int64_t unit0 = PAIR ? (blockIdx.x >> 1) : blockIdx.x;
-  const int64_t ustride = PAIR ? (gridDim.x >> 1) : gridDim.x;
-  const int64_t nunits_wgrad = PAIR ? ((p.N >> 7) + 1) >> 1 : (p.N >> 7);
-  const int64_t total_tiles =
-      p.mode != 1 ? static_cast<int64_t>(tile_off[p.G]) : p.G * nunits_wgrad * (p.K / BN);
+  const int64_t unit0 = blockIdx.x;
+  const int64_t ustride = gridDim.x;
+  const int64_t total_tiles = p.mode != 1 ? static_cast<int64_t>(tile_off[p.G])
+                                          : p.G * (p.N >> 7) * (p.K / BN);
 
   // ------------------------------------------------------------ producer
   if (warp == 0) {
@@ -407,23 +390,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;  // per stage, for the final drain
       bool ok = true;
-      // L2 prefetch cursor, p.prefetch K blocks ahead of the loads: the CTAs
-      // that share a B tile walk its K blocks in lockstep, so without it every
-      // stage would wait for a first-touch DRAM read
-      int64_t pf_t = p.prefetch > 0 ? unit0 : total_tiles, pf_kb = p.prefetch;
-      TileInfo pf;
-      pf.kb_count = 0;
-      if (pf_t < total_tiles) pf = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(pf_t, p, row_off, tile_off, rank);
-      auto pf_normalise = [&]() {
-        while (pf_t < total_tiles && pf_kb >= pf.kb_count) {
-          pf_kb -= pf.kb_count;
-          pf_t += ustride;
-          if (pf_t < total_tiles) pf = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(pf_t, p, row_off, tile_off, rank);
-        }
-      };
-      pf_normalise();
       for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
-        const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
+        const TileInfo ti = map_tile<BN, BK, EPB>(t, p, row_off, tile_off);
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
@@ -437,12 +405,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
           const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
           tma_load_2d(sa, &tmap_a, fb, static_cast<int32_t>(ka * BK), static_cast<int32_t>(ti.a_row));
-          if (PAIR)  // my half of the shared B tile, to both CTAs
-            tma_load_2d_mc(sb + rank * (BN / 2) * BK, &tmap_b, fb, static_cast<int32_t>(kbb * BK),
-                           static_cast<int32_t>(ti.b_row + rank * (BN / 2)), 0x3);
-          else
-            tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * BK),
-                        static_cast<int32_t>(ti.b_row));
+          tma_load_2d(sb, &tmap_b, fb, static_cast<int32_t>(kbb * BK),
+                      static_cast<int32_t>(ti.b_row));
           // first scale tile of this stage along K (MXFP8: tiles of 128 bytes of K)
           const int64_t a_atom = NVF4 ? ka * Cfg::kAtomsK : (ka * BK) >> 7;
           const int64_t b_atom = NVF4 ? kbb * Cfg::kAtomsK : (kbb * BK) >> 7;
@@ -455,14 +419,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
                       512 * Cfg::kAtomsK, fb);
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (pf_t < total_tiles) {
-            const int64_t pka = pf.a_kb0 + pf_kb, pkb = pf.b_kb0 + pf_kb;
-            tma_prefetch_2d(&tmap_a, static_cast<int32_t>(pka * BK), static_cast<int32_t>(pf.a_row));
-            tma_prefetch_2d(&tmap_b, static_cast<int32_t>(pkb * BK),
-                            static_cast<int32_t>(pf.b_row + (PAIR ? rank * (BN / 2) : 0)));
-            ++pf_kb;
-            pf_normalise();
-          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -480,7 +436,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_tiles; t += ustride) {
-        const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
+        const TileInfo ti = map_tile<BN, BK, EPB>(t, p, row_off, tile_off);
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -496,14 +452,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
           const uint32_t ssfb = ssfa + Cfg::kSfaBytes;
           const uint32_t sfa_t = tmem_base + ACC * BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-          if (ti.dup) {  // nothing to compute; release the stage in both CTAs
-            if (PAIR) tc_commit_mc(empty_bar(stage), 0x3);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
           // scale tiles -> TMEM.  A: tile a at column 4a.  B: for K-step a,
           // band i at column a * 4 * (BN/128) + 4i (the bands of one MMA are
           // adjacent, 4 columns each).
@@ -532,11 +480,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
               tc_mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t, sfb_t, accum);
             }
           }
-          // frees the stage (in both CTAs when paired) once these MMAs finish
-          if (PAIR)
-            tc_commit_mc(empty_bar(stage), 0x3);
-          else
-            tc_commit(empty_bar(stage));
+          tc_commit(empty_bar(stage));  // frees the stage once these MMAs finish
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -563,11 +507,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     const uint32_t col0 = 128u * (ew >> 2);
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t t = unit0; t < total_tiles; t += ustride) {
-      const TileInfo ti = map_tile<BN, PAIR, BK, NVF4 ? 2 : 1>(t, p, row_off, tile_off, rank);
+      const TileInfo ti = map_tile<BN, BK, EPB>(t, p, row_off, tile_off);
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
-      const bool has_k = ti.kb_count > 0 && !ti.dup;
+      const bool has_k = ti.kb_count > 0;
       if (has_k) {
         const uint32_t taddr = tmem_base + ((32u * quarter) << 16) + acc * BN + col0;
 #pragma unroll
@@ -581,15 +525,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
         acc = 0;
         acc_phase ^= 1u;
       }
-
-      const int64_t row = ti.c_row + 32 * quarter + lane;
-      if (!ti.dup) epilogue_row<NVF4>(p, ti, row, col0, v, has_k);
+      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k);
     }
   }
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
-  if (PAIR) cluster_sync();  // no multicast or remote arrival targets an exited CTA
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -677,7 +618,6 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
                                                   const int32_t* row_off, const int32_t* prow_off,
                                                   const int32_t* tile_off, uint32_t rank) {
   TileInfo ti;
-  ti.dup = false;
   if (p.mode != 1) {
     int lo = 0, hi = p.G;  // largest g with tile_off[g] <= t
     while (hi - lo > 1) {
@@ -1031,22 +971,19 @@ cudaError_t launch_clusters(Kern kern, int threads, size_t smem, int64_t max_uni
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int BN, int STAGES, int ACC, bool NVF4, bool PAIR, int BK>
+template <int BN, int STAGES, int ACC, bool NVF4, int BK>
 cudaError_t launch_variant(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                            int64_t max_units, int num_sms, cudaStream_t stream) {
   using Cfg = GemmCfg<BN, STAGES, ACC, NVF4, BK>;
-  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4, PAIR, BK>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, ACC, NVF4, BK>;
   const size_t smem = Cfg::smem_bytes(p.G);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (max_units <= 0) return cudaSuccess;
-  if (!PAIR) {
-    const int grid = static_cast<int>(max_units < num_sms ? max_units : num_sms);
-    kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
-    return cudaGetLastError();
-  }
-  return launch_clusters(kern, Cfg::kThreads, smem, max_units, num_sms, stream, ta, tb, p);
+  const int grid = static_cast<int>(max_units < num_sms ? max_units : num_sms);
+  kern<<<grid, Cfg::kThreads, smem, stream>>>(ta, tb, p);
+  return cudaGetLastError();
 }
 
 template <int STAGES, bool NVF4, int BKB>
@@ -1068,23 +1005,20 @@ cudaError_t launch_pair_variant(const CUtensorMap& ta, const CUtensorMap& tb,
 }  // namespace
 
 // Kernel choice.  Default (tile_n = 0): the CTA-pair kernel, 256 x 256
-// units, whenever a stage holds 128 bytes of K (everything but NVFP4 wgrad and
-// NVFP4 fprop with K % 256) and B has at least 256 rows; otherwise the
-// single-CTA kernel.  tile_n = 256 or 128 forces the
-// single-CTA kernel with that tile width (256 needs a width that allows it).
-// pair = 1 selects the single-CTA kernel's multicast variant (two CTAs of a
-// cluster share one B tile).
+// units, whenever B has at least 256 rows; otherwise the single-CTA kernel.
+// tile_n = 256 or 128 forces the single-CTA kernel with that tile width (256
+// needs an output width that allows it); stage_bytes = 128 forces 128-byte K
+// stages where the default would take 256 (MXFP8 fprop with K % 256 == 0).
+// Both overrides exist for the parity tests of every kernel variant.
 cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const uint8_t* a_sf,
                                 const float* a_outer, const void* b_data, const uint8_t* b_sf,
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int pair, int bk, int prefetch,
-                                int inject, uint64_t timeout_ns, int unaligned,
-                                cudaStream_t stream) {
+                                int num_sms, int tile_n, int stage_bytes, int inject,
+                                uint64_t timeout_ns, int unaligned, cudaStream_t stream) {
   GemmParams p;
   p.unaligned = unaligned;
-  p.prefetch = prefetch;
   p.inject = inject;
   p.timeout_ns = timeout_ns;
   p.a_sf = a_sf;
@@ -1118,28 +1052,21 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   const int64_t blk = nvfp4 ? 16 : 32;
   p.a_atoms_row = a_kdim / blk / 4;
   p.b_atoms_row = b_kdim / blk / 4;
-  // bytes of K per pipeline stage; NVFP4 wgrad needs 64 (a 128-row group is
-  // 64 bytes of E2M1 along the contraction)
-  // (and an NVFP4 fprop whose K is not a multiple of 256 elements)
+  const bool pair_kernel = tile_n == 0 && b_rows >= 256;
+  if (unaligned && !(pair_kernel && !nvfp4)) return cudaErrorInvalidValue;
+  // bytes of K per pipeline stage.  NVFP4 wgrad needs 64 (a 128-row group is
+  // 64 bytes of E2M1 along the contraction), and so does an NVFP4 fprop whose
+  // K is not a multiple of 256 elements.  256-byte stages: MXFP8 fprop on the
+  // CTA-pair kernel with K % 256 == 0 (measured: fine-grained fprop 2.5 %
+  // faster, Mixtral fprop unchanged; dgrad lost 2 % with 3 stages instead of
+  // 6 and keeps 128, as does wgrad, whose 128-row groups need it).
   const bool need64 = nvfp4 && (mode == 1 || (K % 256) != 0);
-  // 256-byte stages: MXFP8 fprop on the CTA-pair kernel with K % 256 == 0
-  // (measured: fine-grained fprop 2.5 % faster, Mixtral fprop unchanged; dgrad
-  // lost 2 % with 3 stages instead of 6 and keeps 128, as does wgrad, whose
-  // 128-row groups need it)
-  const bool pair_kernel_default = tile_n == 0 && !pair;
-  const bool wide = !nvfp4 && bk == 0 && (pair_kernel_default || unaligned) && mode == 0 &&
-                    K % 256 == 0 && G * N >= 256;
-  const int BKB = need64 || (bk == 64 && !pair) ? 64 : (wide ? 256 : 128);
-  if (need64) pair = 0;
+  const bool wide = !nvfp4 && stage_bytes == 0 && pair_kernel && mode == 0 && K % 256 == 0;
+  const int BKB = need64 ? 64 : (wide ? 256 : 128);
   p.kb_uniform = mode == 0 ? (nvfp4 ? K / 2 : K) / BKB : (mode == 2 ? N / BKB : 0);
   p.out_cols = mode == 0 ? N : K;
-  const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
 
-  // default: the CTA-pair kernel (256 x 256 units) whenever B spans at least
-  // the two 128-row bands of one unit and the stage size is 128 bytes of K
-  // (or 64 bytes with NVFP4)
-  if (unaligned && !(BKB >= 128 && b_rows >= 256 && !nvfp4)) return cudaErrorInvalidValue;
-  if (unaligned || (tile_n == 0 && !pair && (BKB >= 128 || nvfp4) && b_rows >= 256)) {
+  if (pair_kernel) {
     CUtensorMap ta, tb, tsa, tsb;
     const int atoms = nvfp4 ? BKB / 32 : BKB / 128;  // scale tiles along K per stage and band
     const uint64_t b_bands = static_cast<uint64_t>(b_rows / 128);
@@ -1164,38 +1091,27 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
     return launch_pair_variant<6, false, 128>(ta, tb, tsa, tsb, p, units, num_sms, stream);
   }
 
-  const bool pr = pair != 0;
+  // single-CTA kernel: tile width 256 where asked for (or by default) and the
+  // output width allows it, else 128
+  const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
   const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128, BKB) ||
-      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows,
-                 pr ? bn / 2 : bn, BKB))
+      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows, bn, BKB))
     return cudaErrorInvalidValue;
-
   // upper bound on the work units (device-side group sizes are unknown here)
-  int64_t max_units;
-  if (mode == 1)
-    max_units = G * (pr ? ((N / 128) + 1) / 2 : N / 128) * (K / bn);
-  else
-    max_units = (pr ? ((M_cap / 128) + G + 1) / 2 : M_cap / 128) * (p.out_cols / bn);
-#define MXG_LAUNCH(BN_, S_, A_, NV_)                                                          \
-  return pr ? launch_variant<BN_, S_, A_, NV_, true, 128>(ta, tb, p, max_units, num_sms, stream) \
-            : launch_variant<BN_, S_, A_, NV_, false, 128>(ta, tb, p, max_units, num_sms, stream)
-  if (BKB == 64) {  // half-size stages, twice as many
-    if (bn == 256) {
-      if (nvfp4) return launch_variant<256, 7, 1, true, false, 64>(ta, tb, p, max_units, num_sms, stream);
-      return launch_variant<256, 8, 1, false, false, 64>(ta, tb, p, max_units, num_sms, stream);
-    }
-    if (nvfp4) return launch_variant<128, 10, 2, true, false, 64>(ta, tb, p, max_units, num_sms, stream);
-    return launch_variant<128, 12, 2, false, false, 64>(ta, tb, p, max_units, num_sms, stream);
+  const int64_t max_units = mode == 1 ? G * (N / 128) * (K / bn)
+                                      : (M_cap / 128) * (p.out_cols / bn);
+  if (BKB == 64) {  // NVFP4 with half-size stages, twice as many
+    if (bn == 256) return launch_variant<256, 7, 1, true, 64>(ta, tb, p, max_units, num_sms, stream);
+    return launch_variant<128, 10, 2, true, 64>(ta, tb, p, max_units, num_sms, stream);
   }
   if (nvfp4) {
-    if (bn == 256) MXG_LAUNCH(256, 4, 1, true);
-    MXG_LAUNCH(128, 5, 2, true);
+    if (bn == 256) return launch_variant<256, 4, 1, true, 128>(ta, tb, p, max_units, num_sms, stream);
+    return launch_variant<128, 5, 2, true, 128>(ta, tb, p, max_units, num_sms, stream);
   }
-  if (bn == 256) MXG_LAUNCH(256, 4, 1, false);
-  MXG_LAUNCH(128, 6, 2, false);
-#undef MXG_LAUNCH
+  if (bn == 256) return launch_variant<256, 4, 1, false, 128>(ta, tb, p, max_units, num_sms, stream);
+  return launch_variant<128, 6, 2, false, 128>(ta, tb, p, max_units, num_sms, stream);
 }
 
 }  // namespace mxg

@@ -2,8 +2,6 @@
 // device checks and kernel dispatch.  Host code only; no allocation, no
 // synchronisation.
 #include <atomic>
-#include <cstdlib>
-#include <cstring>
 #include <mutex>
 
 #include "mxg_device.cuh"
@@ -31,9 +29,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 const float* b_outer, const int64_t* group_ws, int G, int64_t M_cap,
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
-                                int num_sms, int tile_n, int pair, int bk, int prefetch,
-                                int inject, uint64_t timeout_ns, int unaligned,
-                                cudaStream_t stream);
+                                int num_sms, int tile_n, int stage_bytes, int inject,
+                                uint64_t timeout_ns, int unaligned, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -79,29 +76,19 @@ mxg_status_t launched(cudaError_t e, uint64_t n) {
   return MXG_OK;
 }
 
-int env_tile_n() {
-  const char* s = std::getenv("MXG_GEMM_TILE_N");
-  return s ? std::atoi(s) : 0;
-}
+// The kernels index rows (and the padded rows of groups of any size) with
+// 32-bit integers in their group tables.
+constexpr int64_t kMaxRows = 0x7FFFFF80LL;
 
-// Bytes of K per GEMM pipeline stage: 0 (default: 256 for MXFP8 fprop on the
-// CTA-pair kernel when K % 256 == 0, else 128), 128 or 64.
-int env_bk() {
-  const char* s = std::getenv("MXG_GEMM_BK");
-  return s ? std::atoi(s) : 0;
-}
-
-// L2 prefetch distance of the GEMM producer, in K blocks (default off: on
-// GB300 the extra copy instructions cost more than the latency they hide).
-int env_prefetch() {
-  const char* s = std::getenv("MXG_GEMM_PREFETCH");
-  return s ? std::atoi(s) : 0;
-}
-
-// 2-CTA clusters sharing the B tile (default off until enabled here).
-int env_pair() {
-  const char* s = std::getenv("MXG_GEMM_PAIR");
-  return s ? (std::atoi(s) != 0) : 0;
+// Arguments of the offsets entry points.  Bounds on the multiplier (2^31)
+// and on the capacity (2^62, and capacity * last_dim within int64) keep every
+// product the kernel forms -- sanitised rows times the multiplier, offsets
+// times last_dim -- inside 64 bits.
+bool offsets_args_ok(const void* sizes, const int64_t* ws, int G, int64_t multiplier,
+                     int64_t last_dim, int64_t rows_capacity) {
+  return sizes != nullptr && ws != nullptr && G >= 1 && G <= 65536 && multiplier >= 1 &&
+         multiplier <= (1LL << 31) && last_dim >= 1 && rows_capacity >= 0 &&
+         rows_capacity <= (1LL << 62) && rows_capacity <= INT64_MAX / last_dim;
 }
 
 }  // namespace
@@ -115,8 +102,7 @@ size_t mxg_offsets_workspace_bytes(int G) {
 mxg_status_t mxg_group_offsets(const void* sizes, int sizes_is_int64, int G, int64_t multiplier,
                                int64_t last_dim, int64_t rows_capacity, int64_t* ws,
                                int32_t* dev_status, mxg_stream_t stream) {
-  if (sizes == nullptr || ws == nullptr || G < 1 || G > 65536 || multiplier < 1 || last_dim < 1 ||
-      rows_capacity < 0)
+  if (!offsets_args_ok(sizes, ws, G, multiplier, last_dim, rows_capacity))
     return MXG_ERR_INVALID_ARG;
   int sms = 0;
   const mxg_status_t st = current_device(&sms);
@@ -131,8 +117,7 @@ mxg_status_t mxg_group_offsets_unaligned(const void* sizes, int sizes_is_int64, 
                                          int64_t multiplier, int64_t last_dim,
                                          int64_t rows_capacity, int64_t* ws, int32_t* dev_status,
                                          mxg_stream_t stream) {
-  if (sizes == nullptr || ws == nullptr || G < 1 || G > 65536 || multiplier < 1 || last_dim < 1 ||
-      rows_capacity < 0)
+  if (!offsets_args_ok(sizes, ws, G, multiplier, last_dim, rows_capacity))
     return MXG_ERR_INVALID_ARG;
   int sms = 0;
   const mxg_status_t st = current_device(&sms);
@@ -161,6 +146,7 @@ mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
       (col && (q_col == nullptr || sf_col == nullptr)))
     return MXG_ERR_INVALID_ARG;
   if (!mult128(rows_capacity) || !mult128(cols) || cols == 0) return MXG_ERR_ALIGNMENT;
+  if (rows_capacity + 128 * static_cast<int64_t>(G) > kMaxRows) return MXG_ERR_INVALID_ARG;
   if (!aligned16(x) || (row && (!aligned16(q_row) || !aligned16(sf_row))) ||
       (col && (!aligned16(q_col) || !aligned16(sf_col))))
     return MXG_ERR_ALIGNMENT;
@@ -232,8 +218,8 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
                                       const int64_t* group_ws, int G, int64_t M_cap, int64_t N,
                                       int64_t K, const float* alpha, const float* beta,
                                       const float* bias, void* C, mxg_out_t out_type,
-                                      int32_t* dev_status, int inject,
-                                      uint64_t timeout_ns, mxg_stream_t stream,
+                                      int32_t* dev_status, int tile_n, int stage_bytes,
+                                      int inject, uint64_t timeout_ns, mxg_stream_t stream,
                                       int unaligned) {
   if (A == nullptr || B == nullptr || C == nullptr || group_ws == nullptr || G < 1 || G > 1024)
     return MXG_ERR_INVALID_ARG;
@@ -253,7 +239,9 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   if (!mult128(M_cap) || !mult128(N) || !mult128(K) || N == 0 || K == 0)
     return MXG_ERR_ALIGNMENT;
 
-  if (M_cap > 0x7FFFFF80LL || N * static_cast<int64_t>(G) > 0x7FFFFF80LL) return MXG_ERR_INVALID_ARG;
+  if (M_cap + (unaligned ? 128 * static_cast<int64_t>(G) : 0) > kMaxRows ||
+      N * static_cast<int64_t>(G) > kMaxRows)
+    return MXG_ERR_INVALID_ARG;
   if (!aligned16(A->data) || !aligned16(A->scale) || !aligned16(B->data) || !aligned16(B->scale) ||
       !aligned16(C))
     return MXG_ERR_ALIGNMENT;
@@ -264,9 +252,8 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   return launched(mxg::launch_grouped_gemm(
                       nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, env_tile_n(), env_pair(),
-                      env_bk(), env_prefetch(), inject,
-                      timeout_ns, unaligned, reinterpret_cast<cudaStream_t>(stream)),
+                      out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, tile_n, stage_bytes,
+                      inject, timeout_ns, unaligned, reinterpret_cast<cudaStream_t>(stream)),
                   1);
 }
 
@@ -279,20 +266,23 @@ mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_
   (void)workspace;
   (void)workspace_bytes;
   return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                           out_type, dev_status, 0, mxg::kDefaultWaitNs, stream, 0);
+                           out_type, dev_status, 0, 0, 0, mxg::kDefaultWaitNs, stream, 0);
 }
 
 mxg_status_t mxg_grouped_gemm_debug(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
                                     const mxg_operand_t* B, const int64_t* group_ws, int G,
                                     int64_t M_cap, int64_t N, int64_t K, const float* alpha,
                                     const float* beta, const float* bias, void* C,
-                                    mxg_out_t out_type, int32_t* dev_status, int inject_flags,
-                                    int64_t wait_timeout_ns, mxg_stream_t stream) {
+                                    mxg_out_t out_type, int32_t* dev_status, int tile_n,
+                                    int stage_bytes, int inject_flags, int64_t wait_timeout_ns,
+                                    mxg_stream_t stream) {
   if (wait_timeout_ns < 0 || (inject_flags & ~1)) return MXG_ERR_INVALID_ARG;
+  if ((tile_n != 0 && tile_n != 128 && tile_n != 256) || (stage_bytes != 0 && stage_bytes != 128))
+    return MXG_ERR_INVALID_ARG;
   const uint64_t t = wait_timeout_ns == 0 ? mxg::kDefaultWaitNs
                                           : static_cast<uint64_t>(wait_timeout_ns);
   return grouped_gemm_impl(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
-                           out_type, dev_status, inject_flags, t, stream, 0);
+                           out_type, dev_status, tile_n, stage_bytes, inject_flags, t, stream, 0);
 }
 
 mxg_status_t mxg_grouped_gemm_unaligned(mxg_gemm_mode_t mode, const mxg_operand_t* A,
@@ -302,7 +292,7 @@ mxg_status_t mxg_grouped_gemm_unaligned(mxg_gemm_mode_t mode, const mxg_operand_
                                         mxg_out_t out_type, int32_t* dev_status,
                                         mxg_stream_t stream) {
   return grouped_gemm_impl(MXG_MXFP8_E4M3, mode, A, B, group_ws, G, M_cap, N, K, alpha, beta, bias,
-                           C, out_type, dev_status, 0, mxg::kDefaultWaitNs, stream, 1);
+                           C, out_type, dev_status, 0, 0, 0, mxg::kDefaultWaitNs, stream, 1);
 }
 
 size_t mxg_grouped_gemm_workspace_bytes(mxg_format_t fmt, mxg_gemm_mode_t mode, int G,

@@ -31,16 +31,24 @@ __global__ void __launch_bounds__(32, 1)
     if (g < G) {
       s = is_int64 ? static_cast<const int64_t*>(sizes)[g]
                    : static_cast<int64_t>(static_cast<const int32_t*>(sizes)[g]);
-      s *= mult;
-      if (s < 0) {
+      if (s < 0) {  // rows = size * multiplier with multiplier >= 1: negative iff size is
         bits |= MXG_DEV_NEG_SIZE;
         s = 0;
+      } else if (s > INT64_MAX / mult) {
+        // size * multiplier does not fit in 64 bits.  The host bounds
+        // multiplier <= 2^31 and cap <= 2^62, so the exact product is far
+        // above cap + 127: its rounded value is clamped to cap.  Whether it
+        // is a multiple of 128 follows from the factors modulo 128.
+        if (round128 && (((s & 127) * (mult & 127)) & 127)) bits |= MXG_DEV_MISALIGNED;
+        s = cap;
+      } else {
+        s *= mult;
+        if (round128 && (s & 127)) {
+          bits |= MXG_DEV_MISALIGNED;
+          s &= ~static_cast<int64_t>(127);
+        }
+        if (s > cap) s = cap;  // keeps the running sum far from overflow
       }
-      if (round128 && (s & 127)) {
-        bits |= MXG_DEV_MISALIGNED;
-        s &= ~static_cast<int64_t>(127);
-      }
-      if (s > cap) s = cap;  // keeps the running sum far from overflow
     }
     // inclusive warp scan of s
     int64_t incl = s;

@@ -71,7 +71,7 @@ def load() -> ctypes.CDLL:
         L.mxg_grouped_gemm_debug.restype = c_int
         L.mxg_grouped_gemm_debug.argtypes = [c_int, c_int, ctypes.POINTER(Operand),
                                              ctypes.POINTER(Operand), vp, c_int, i64, i64, i64, vp,
-                                             vp, vp, vp, c_int, vp, c_int, i64, vp]
+                                             vp, vp, vp, c_int, vp, c_int, c_int, c_int, i64, vp]
         L.mxg_grouped_gemm_workspace_bytes.restype = sz
         L.mxg_grouped_gemm_workspace_bytes.argtypes = [c_int, c_int, c_int, i64, i64]
         L.mxg_dequantize.restype = c_int
@@ -166,16 +166,16 @@ def mxg_grouped_gemm(fmt: int, mode: int, A: tuple, B: tuple, group_ws: torch.Te
 
 def mxg_grouped_gemm_debug(fmt: int, mode: int, A: tuple, B: tuple, group_ws, G: int, M_cap: int,
                            N: int, K: int, alpha=None, beta=None, C=None,
-                           out_type: int = MXG_OUT_F32, dev_status=None, inject_flags: int = 0,
-                           wait_timeout_ns: int = 0, stream=None, bias=None) -> None:
+                           out_type: int = MXG_OUT_F32, dev_status=None, tile_n: int = 0,
+                           stage_bytes: int = 0, inject_flags: int = 0, wait_timeout_ns: int = 0,
+                           stream=None, bias=None) -> None:
     a = Operand(_p(A[0]), _p(A[1]), _p(A[2]) if len(A) > 2 else None)
     b = Operand(_p(B[0]), _p(B[1]), _p(B[2]) if len(B) > 2 else None)
     _check("mxg_grouped_gemm_debug",
            load().mxg_grouped_gemm_debug(fmt, mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws),
                                          G, M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C),
-                                         out_type,
-                                         _p(dev_status), inject_flags, wait_timeout_ns,
-                                         _s(stream)))
+                                         out_type, _p(dev_status), tile_n, stage_bytes,
+                                         inject_flags, wait_timeout_ns, _s(stream)))
 
 
 def mxg_grouped_gemm_workspace_bytes(fmt: int, mode: int, G: int, M_cap: int, N: int) -> int:

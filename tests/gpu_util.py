@@ -2,7 +2,6 @@
 the oracle on the same seeded inputs.  Imported by tests only."""
 from __future__ import annotations
 
-import os
 
 import numpy as np
 import pytest
@@ -79,24 +78,40 @@ def normwise_errors(got: np.ndarray, ref: np.ndarray, offs, rows=None):
     return np.array(errs)
 
 
-class tile_n:
-    """Context manager forcing the GEMM's output tile width (MXG_GEMM_TILE_N)."""
+class gemm_override:
+    """Context manager that routes mxg.mxg_grouped_gemm through the test entry
+    point mxg_grouped_gemm_debug with a forced kernel choice: tile_n = 256 or
+    128 selects the single-CTA kernel with that tile width, stage_bytes = 128
+    forces 128-byte K stages.  With neither set, calls are left unchanged."""
 
-    def __init__(self, n):
-        self.n = n
+    def __init__(self, tile_n=None, stage_bytes=None):
+        self.tile_n = tile_n or 0
+        self.stage_bytes = stage_bytes or 0
 
     def __enter__(self):
-        self.old = os.environ.get("MXG_GEMM_TILE_N")
-        if self.n is None:
-            os.environ.pop("MXG_GEMM_TILE_N", None)
-        else:
-            os.environ["MXG_GEMM_TILE_N"] = str(self.n)
+        self.orig = mxg.mxg_grouped_gemm
+        if not self.tile_n and not self.stage_bytes:
+            return self
+        orig_debug = mxg.mxg_grouped_gemm_debug
+        tn, sb = self.tile_n, self.stage_bytes
+
+        def forced(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha=None, beta=None, C=None,
+                   out_type=mxg.MXG_OUT_F32, workspace=None, workspace_bytes=0, dev_status=None,
+                   stream=None, bias=None):
+            orig_debug(fmt, mode, A, B, group_ws, G, M_cap, N, K, alpha=alpha, beta=beta, C=C,
+                       out_type=out_type, dev_status=dev_status, tile_n=tn, stage_bytes=sb,
+                       stream=stream, bias=bias)
+
+        mxg.mxg_grouped_gemm = forced
+        return self
 
     def __exit__(self, *a):
-        if self.old is None:
-            os.environ.pop("MXG_GEMM_TILE_N", None)
-        else:
-            os.environ["MXG_GEMM_TILE_N"] = self.old
+        mxg.mxg_grouped_gemm = self.orig
+
+
+def tile_n(n):
+    """gemm_override forcing the single-CTA kernel's tile width (None: default)."""
+    return gemm_override(tile_n=n)
 
 
 def fprop_case(wl: workloads.Workload, layout_x=mxg.MXG_ROWWISE, out_type=mxg.MXG_OUT_F32,

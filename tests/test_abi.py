@@ -53,6 +53,35 @@ def test_offsets_argument_errors(lib):
 
 
 @no_device_only
+def test_offsets_bounds_keep_products_in_int64(lib):
+    """Multiplier above 2^31, capacity above 2^62, capacity * last_dim past
+    int64: refused, for both offsets entry points."""
+    for f in (lib.mxg_group_offsets, lib.mxg_group_offsets_unaligned):
+        assert f(FAKE, 1, 4, (1 << 31) + 1, 128, 512, FAKE, None, None) == 1
+        assert f(FAKE, 1, 4, 1, 128, (1 << 62) + 128, FAKE, None, None) == 1
+        assert f(FAKE, 1, 4, 1, 1 << 40, 1 << 24, FAKE, None, None) == 1
+
+
+@no_device_only
+def test_unaligned_quantize_rejects_padded_rows_past_int32(lib):
+    q = lib.mxg_group_quantize_unaligned
+    # 0x7FFFFF00 + 128 * 1024 padded rows do not fit the kernels' 32-bit row tables
+    assert q(3, FAKE, 0x7FFFFF00, 128, FAKE, 1024, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+
+
+@no_device_only
+def test_debug_entry_validates_its_overrides(lib):
+    op = mxg.Operand(FAKE, FAKE, None)
+    r = ctypes.byref
+    d = lib.mxg_grouped_gemm_debug
+    args = (1, 0, r(op), r(op), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None)
+    assert d(*args, 64, 0, 0, 0, None) == 1     # tile width 64 does not exist
+    assert d(*args, 0, 256, 0, 0, None) == 1    # only 128-byte stages can be forced
+    assert d(*args, 0, 0, 2, 0, None) == 1      # unknown inject bit
+    assert d(*args, 0, 0, 0, -1, None) == 1     # negative wait bound
+
+
+@no_device_only
 def test_quantize_argument_errors(lib):
     L = lib
     q = L.mxg_group_quantize

@@ -32,6 +32,54 @@ def test_offsets_parity(G, dtype):
     assert int(st.item()) == rst == 0
 
 
+def _offsets_by_definition(sizes, mult, last_dim, cap, round128=True):
+    """The sanitised workspace from its definition in exact (Python) integer
+    arithmetic: rows = size * multiplier, negative -> 0, rounded down to 128,
+    the running sum kept within the capacity."""
+    bits, kept, p = 0, [], 0
+    for s in sizes:
+        v = int(s) * mult
+        if v < 0:
+            bits |= mxg.MXG_DEV_NEG_SIZE
+            v = 0
+        if round128 and v % 128:
+            bits |= mxg.MXG_DEV_MISALIGNED
+            v -= v % 128
+        v = min(v, cap)
+        before, p = min(p, cap), p + v
+        if p > cap and v > 0:
+            bits |= mxg.MXG_DEV_SUM_OVER_CAPACITY
+        kept.append(min(p, cap) - before)
+    offs = np.concatenate([[0], np.cumsum(kept)]) * last_dim
+    return np.concatenate([np.array(kept, np.int64), offs.astype(np.int64)]), bits
+
+
+def test_offsets_definition_matches_the_oracle():
+    """The exact-integer definition above agrees with the oracle wherever the
+    oracle's 64-bit products do not overflow (so it can stand for the oracle
+    on the overflow cases below)."""
+    rng = np.random.default_rng(5)
+    for mult in (1, 3, 128):
+        sizes = rng.integers(-300, 3000, 40)
+        ref, rst = oracle.group_offsets(sizes, mult, 4096, 1 << 18)
+        mine, bits = _offsets_by_definition(sizes, mult, 4096, 1 << 18)
+        assert np.array_equal(ref, mine) and rst == bits
+
+
+@pytest.mark.parametrize("mult", [1, 4, 1 << 31])
+def test_offsets_huge_sizes_do_not_overflow(mult):
+    """Sizes whose product with the multiplier overflows int64 are clamped
+    to the capacity like any other oversize group, with the status bits of
+    the exact product."""
+    sizes = torch.tensor([(1 << 62) + 5, -5, 384, 1000, (1 << 40) + 1, 1 << 61],
+                         dtype=torch.int64)
+    cap = 1 << 20
+    ws, st = gpu_offsets(sizes, 4096, cap, mult=mult)
+    ref, bits = _offsets_by_definition(sizes.tolist(), mult, 4096, cap)
+    assert np.array_equal(ws.cpu().numpy(), ref)
+    assert int(st.item()) == bits
+
+
 def test_offsets_multiplier():
     sizes = torch.tensor([1, 0, 3, 2, 7], dtype=torch.int32)
     ws, st = gpu_offsets(sizes, 7168, 1 << 20, mult=128)

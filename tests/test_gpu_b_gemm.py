@@ -15,7 +15,8 @@ import oracle
 from moe_grouped_block_gb300 import mxg, workloads
 
 from gpu_util import (DEV, fprop_case, gpu_mxfp8, gpu_offsets, normwise_errors, oracle_fprop,
-                      oracle_quantized_operands, require_gpu, tile_n, u8)
+                      oracle_quantized_operands, require_gpu, tile_n, u8,
+                      gemm_override)
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
@@ -280,16 +281,15 @@ def test_dgrad_scaled(tn, K):
 
 
 @pytest.mark.parametrize("N", [384, 512, 768])
-@pytest.mark.parametrize("bk", [None, "128"])
-def test_stage_width_fprop_and_dgrad(N, bk, monkeypatch):
+@pytest.mark.parametrize("bk", [None, 128])
+def test_stage_width_fprop_and_dgrad(N, bk):
     """The MXFP8 CTA-pair kernel takes 256 bytes of K per fprop stage when K
-    is a multiple of 256 and 128 otherwise (or when MXG_GEMM_BK=128 forces it);
-    dgrad keeps 128.  Both widths, with one and several stages, and dgrad over
-    the same contraction lengths, match the oracle."""
-    if bk is not None:
-        monkeypatch.setenv("MXG_GEMM_BK", bk)
+    is a multiple of 256 and 128 otherwise (or when the test entry point
+    forces 128); dgrad keeps 128.  Both widths, with one and several stages,
+    and dgrad over the same contraction lengths, match the oracle."""
     wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=N, N=512)
-    case, offs, rows, ref = _run_fprop(wl)
+    with gemm_override(stage_bytes=bk):
+        case, offs, rows, ref = _run_fprop(wl)
     errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
     assert errs.max() <= TOL, errs
     _dgrad_check(None, 512, N)

@@ -256,7 +256,6 @@ def test_bounded_wait_runs_out_and_the_device_stays_usable(tn):
     report MXG_DEV_TIMEOUT, drain, free tensor memory and return; the next
     normal launch on the same context must be correct."""
     import time
-    from gpu_util import tile_n
     G, N, K, R = 4, 256, 256, 1024
     x_h = workloads.random_bf16((R, K), seed=51)
     w_h = workloads.random_bf16((G * N, K), seed=52, scale=0.02)
@@ -272,17 +271,17 @@ def test_bounded_wait_runs_out_and_the_device_stays_usable(tn):
     B = (qw["q_row"], qw["sf_row"], None)
     C = torch.zeros((R, N), dtype=torch.float32, device=DEV)
     bad = torch.zeros(1, dtype=torch.int32, device=DEV)
-    with tile_n(tn):
-        t0 = time.time()
-        mxg.mxg_grouped_gemm_debug(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, C=C,
-                                   dev_status=bad, inject_flags=1, wait_timeout_ns=20_000_000)
-        torch.cuda.synchronize()
-        assert time.time() - t0 < 10.0
-        assert int(bad.item()) & mxg.MXG_DEV_TIMEOUT
-        # the context is intact: a normal launch is correct
-        mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, C=C,
-                             dev_status=st)
-        torch.cuda.synchronize()
+    t0 = time.time()
+    mxg.mxg_grouped_gemm_debug(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, C=C,
+                               dev_status=bad, tile_n=tn or 0, inject_flags=1,
+                               wait_timeout_ns=20_000_000)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 10.0
+    assert int(bad.item()) & mxg.MXG_DEV_TIMEOUT
+    # the context is intact: a normal launch is correct
+    mxg.mxg_grouped_gemm_debug(mxg.MXG_MXFP8_E4M3, mxg.MXG_FPROP_TN, A, B, ws, G, R, N, K, C=C,
+                               dev_status=st, tile_n=tn or 0)
+    torch.cuda.synchronize()
     assert int(st.item()) == 0
     _, _, offs, ref = _oracle_fprop(x_h, w_h, sizes.numpy(), G, N, K, R)
     errs = normwise_errors(C.cpu().numpy().astype(np.float64), ref, offs)
