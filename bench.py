@@ -2,12 +2,13 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mxg|reference]
                     [--config mixtral_fprop_mxfp8|finegrained_fprop_mxfp8|wgrad_mxfp8|
-                              rowscaled_fprop_nvfp4|tiny_fprop_mxfp8] [--out bf16|f32]
+                              rowscaled_fprop_nvfp4|wgrad_nvfp4|dgrad_mxfp8|...]
+                    [--configs a,b,c] [--out bf16|f32]
 
 One step is one pass of the whole path over one batch of synthetic input:
   fprop:  group offsets -> quantize X (MXFP8 rowwise + transposed colwise, or
           row-scaled NVFP4) -> quantize W (rowwise) -> grouped GEMM fprop
-  wgrad:  group offsets -> quantize X and dY (MXFP8 colwise, transposed) ->
+  wgrad:  group offsets -> quantize X and dY (colwise, transposed) ->
           grouped GEMM wgrad
 The metric is grouped quant+GEMM TFLOP/s: 2*M*N*K algorithmic FLOP of the
 GEMM over the time of the whole step, with the inputs resident in HBM.  Each
@@ -16,11 +17,18 @@ step is timed with CUDA events on the launching stream; L2 is flushed (a
 measurement through the same C-ABI calls with the inputs copied from pinned
 host memory and the output copied back inside the timed region.
 
+The headline line is the Mixtral-shaped fprop workload; on one GPU the other
+workloads of the metric (--configs: fine-grained fprop, wgrad, row-scaled
+NVFP4 fprop by default) are timed after it the same way and reported under
+"configs", each with its per-kernel times, GEMM roofline and the oracle's
+timing.
+
 For N > 1 (torchrun) every rank runs an independent replica on its own GPU
 and its own seeded batch (the path has no exchange step); the job value is the
 FLOP of all ranks over the slowest rank's time.  ``--impl reference`` times
-the CPU oracle (the only other implementation there is) on a bounded sample
-of the same workload, on rank 0 only.
+the CPU oracle (the only other implementation there is) on rank 0 only, each
+step a fixed sample of the workload -- the sample this arm's cpu_baseline
+times too.
 """
 from __future__ import annotations
 
@@ -39,6 +47,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "grouped quant+GEMM TFLOP/s (frac of dense MXFP8 peak); quantize HBM GB/s"
+# measured after the headline workload and reported under "configs"
+EXTRA_CONFIGS = ("finegrained_fprop_mxfp8", "wgrad_mxfp8", "rowscaled_fprop_nvfp4")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -52,7 +62,20 @@ def load_peaks():
 
 
 GEMM_SOURCES = ("gemm.cu", "mxg_device.cuh", "mxg_host.h", "tmap.cu")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "grouped_gemm_pair_kernel_dram_traffic.md")
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of one
+# full-size GEMM launch per workload, from single-pass ncu captures of
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+#       --clock-control none -k regex:grouped_gemm -s 3 -c 1
+#       python bench.py --config <workload> --steps 1 --warmup 3 --no-cpu-baseline --no-e2e
+#       --configs ''
+# taken on the GEMM sources and compile flags whose digest is "digest"; after
+# any change to either, "traffic" is reported as null until the counters are
+# taken again.
+GEMM_DRAM_TRAFFIC = {
+    "digest": None,
+    "bytes": {},
+}
 
 
 def code_only(text: str) -> str:
@@ -65,40 +88,26 @@ def code_only(text: str) -> str:
 
 
 def gemm_source_digest() -> str:
-    """sha256 over the GEMM kernel's sources (code only, in a fixed order): a
-    DRAM traffic figure is reported only while the kernel it was measured on is
-    unchanged."""
+    """sha256 over the GEMM kernel's sources (code only, in a fixed order) and
+    the nvcc flags the library is built with: a DRAM traffic figure is
+    reported only while the kernel it was measured on is unchanged."""
     import hashlib
+    from moe_grouped_block_gb300 import build as mxg_build
     h = hashlib.sha256()
     for f in GEMM_SOURCES:
         with open(os.path.join(ROOT, "moe_grouped_block_gb300", "csrc", f)) as fh:
             h.update(code_only(fh.read()).encode())
+    h.update(" ".join(mxg_build.ARCH + mxg_build.NVCC_FLAGS).encode())
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes (read + write) of one GEMM launch of this workload, from the
-    committed ncu summary, or None if there is none or the sources changed
-    since it was taken.  The summary's table rows read
-    `| workload | kernel | read bytes | write bytes | traffic bytes | ... |` and
-    it carries a line `sources sha256: <hex>`."""
-    if not os.path.exists(TRAFFIC_SUMMARY):
+def measured_traffic(workload: str, table=None):
+    """DRAM bytes (read + write) of one GEMM launch of this workload, or None
+    if none was measured or the kernel changed since."""
+    table = GEMM_DRAM_TRAFFIC if table is None else table
+    if table.get("digest") != gemm_source_digest():
         return None
-    text = open(TRAFFIC_SUMMARY).read()
-    digest = None
-    for line in text.splitlines():
-        if line.startswith("sources sha256:"):
-            digest = line.split(":", 1)[1].strip().strip("`")
-    if digest != gemm_source_digest():
-        return None
-    for line in text.splitlines():
-        cells = [c.strip().strip("`") for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 5 and cells[0] == workload:
-            try:
-                return int(cells[4])
-            except ValueError:
-                return None
-    return None
+    return table.get("bytes", {}).get(workload)
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
@@ -544,8 +553,8 @@ def gemm_roofline(gemm_name, flops, gemm_bytes, gemm_ms, peaks, peak_src, nvfp4,
                   peak_src, 6 if nvfp4 else 2, peak_src),
               "traffic": traffic,
               "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size "
-                                "launch (profiles/grouped_gemm_pair_kernel_dram_traffic.md); "
-                                "null when the kernel changed since",
+                                "launch (GEMM_DRAM_TRAFFIC in bench.py); null when the kernel "
+                                "changed since",
               "algorithmic_bytes": gemm_bytes, "algorithmic_flop": flops,
               "t_tensor_roofline_ms": round(t_tensor_ms, 5), "t_hbm_roofline_ms": round(t_hbm_ms, 5),
               "t_roofline_over_t": round(max(t_tensor_ms, t_hbm_ms) / gemm_ms, 4)}
@@ -558,27 +567,19 @@ def gemm_roofline(gemm_name, flops, gemm_bytes, gemm_ms, peaks, peak_src, nvfp4,
             "unit": "TFLOP/s", "frac": round(tflops / peak_tc, 4), **common}
 
 
-def run_mxg(args, wl, ws_world, rank, local):
+def time_path(path, args, steps, dist, dev, flush, stream):
+    """Warm-up, one CUDA graph per stage, then `steps` timed steps with CUDA
+    events around every stage's replay on `stream` (L2 flushed before each
+    step, outside the events).  Returns per-stage times, step times, the
+    number of library kernels launched in the timed region, the timing note
+    and the clock record of the timed region."""
     import torch
     from moe_grouped_block_gb300 import mxg
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist = None
-    if ws_world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    path = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue)
     stages = path.stages()
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        for _, fn in stages:
-            fn()
-
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        step()
+        for _, fn in stages:
+            fn()
     torch.cuda.synchronize()
     if int(path.status.item()) != 0:
         raise RuntimeError("device status %d after warm-up" % int(path.status.item()))
@@ -605,18 +606,17 @@ def run_mxg(args, wl, ws_world, rank, local):
             graphs, graph_note = None, "graph capture failed (%s); eager launches timed" % e
             torch.cuda.synchronize()
 
-    # ---- timed region: K steps, per-step and per-kernel CUDA events
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in stages] for _ in range(args.steps)]
+           for _ in stages] for _ in range(steps)]
     uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
-    clocks = ClockSampler(local, str(uuid) if uuid is not None else None)
+    clocks = ClockSampler(dev.index or 0, str(uuid) if uuid is not None else None)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = mxg.mxg_launch_count()
     t_wall = time.perf_counter()
-    for s in range(args.steps):
+    for s in range(steps):
         flush.fill_(1.0)
         for i, ((name, fn), (e0, e1)) in enumerate(zip(stages, ev[s])):
             e0.record(stream)
@@ -630,31 +630,23 @@ def run_mxg(args, wl, ws_world, rank, local):
     if dist:
         dist.barrier()
     # graph replays do not pass through the C ABI: count what one capture launched
-    launches = (graph_launches * args.steps if graphs is not None
+    launches = (graph_launches * steps if graphs is not None
                 else mxg.mxg_launch_count() - launches0)
     clk = clocks.stop()
-    per_kernel = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
-                  for i, (name, _) in enumerate(stages)}
-    step_ms = [ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(args.steps)]
-    ms = max_over_ranks(float(np.mean(step_ms)), dist, dev)
-    ms_median = max_over_ranks(float(np.median(step_ms)), dist, dev)
     if int(path.status.item()) != 0:
         raise RuntimeError("device status %d" % int(path.status.item()))
+    per_kernel = {name: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)]
+                  for i, (name, _) in enumerate(stages)}
+    step_ms = [ev[s][0][0].elapsed_time(ev[s][-1][1]) for s in range(steps)]
+    timing = graph_note or ("CUDA events around CUDA-graph replays (one graph per kernel)"
+                            if graphs is not None else "CUDA events around eager launches")
+    return {"stages": stages, "per_kernel": per_kernel, "step_ms": step_ms,
+            "launches": int(launches), "timing": timing, "clocks": clk, "wall_s": t_wall}
 
-    # ---- e2e: host buffers, copies inside the timed region
-    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else measure_e2e(path, step, args, dist, dev,
-                                                                      flush, stream)
-    e2e_pipe_ms = None
-    if not args.no_e2e:
-        path2 = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue,
-                     inputs=path.host)
-        if path.bias is not None:  # the same epilogue operands in both sets
-            path2.bias.copy_(path.bias)
-            path2.alpha.copy_(path.alpha)
-        e2e_pipe_ms = measure_e2e_pipelined([path, path2], args, dist, dev)
-        del path2
 
-    peaks, peak_src = load_peaks()
+def kernel_table(path, wl, per_kernel, peaks):
+    """Per-stage mean ms, algorithmic GB/s and HBM fraction (and TFLOP/s for
+    the GEMM), and the GEMM's roofline object."""
     flops = wl.flops()
     kernels = {}
     for name, times in per_kernel.items():
@@ -669,10 +661,51 @@ def run_mxg(args, wl, ws_world, rank, local):
         kernels[name] = d
     gemm_name = [n for n in per_kernel if n.startswith("grouped_gemm")][0]
     gemm_ms = float(np.mean(per_kernel[gemm_name]))
-    nvfp4 = wl.fmt == "nvfp4"
+    return kernels, gemm_name, gemm_ms
+
+
+def run_mxg(args, wl, ws_world, rank, local):
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if ws_world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    path = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peaks, peak_src = load_peaks()
+
+    # ---- timed region: K steps, per-step and per-kernel CUDA events
+    r = time_path(path, args, args.steps, dist, dev, flush, stream)
+    stages = r["stages"]
+    ms = max_over_ranks(float(np.mean(r["step_ms"])), dist, dev)
+    ms_median = max_over_ranks(float(np.median(r["step_ms"])), dist, dev)
+
+    def step():
+        for _, fn in stages:
+            fn()
+
+    # ---- e2e: host buffers, copies inside the timed region
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else measure_e2e(path, step, args, dist, dev,
+                                                                      flush, stream)
+    e2e_pipe_ms = None
+    if not args.no_e2e:
+        path2 = Path(wl, args.out == "bf16", dev, rank=rank, epilogue=args.epilogue,
+                     inputs=path.host)
+        if path.bias is not None:  # the same epilogue operands in both sets
+            path2.bias.copy_(path.bias)
+            path2.alpha.copy_(path.alpha)
+        e2e_pipe_ms = measure_e2e_pipelined([path, path2], args, dist, dev)
+        del path2
+
+    flops = wl.flops()
+    kernels, gemm_name, gemm_ms = kernel_table(path, wl, r["per_kernel"], peaks)
     roofline = gemm_roofline(gemm_name, flops, path.kernel_bytes(gemm_name), gemm_ms, peaks,
-                             peak_src, nvfp4, measured_traffic(wl.name))
+                             peak_src, wl.fmt == "nvfp4", measured_traffic(wl.name))
     value = job_tflops(flops, ws_world, ms)
+    nvfp4 = wl.fmt == "nvfp4"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws_world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -684,9 +717,7 @@ def run_mxg(args, wl, ws_world, rank, local):
                    "mode": wl.mode, "out": args.out, "epilogue": args.epilogue,
                    "step": " -> ".join(n for n, _ in stages),
                    "l2": "flushed before every timed step (512 MB write); inputs also exceed L2",
-                   "timing": graph_note or ("CUDA events around CUDA-graph replays (one graph per "
-                                            "kernel)" if graphs is not None else
-                                            "CUDA events around eager launches"),
+                   "timing": r["timing"],
                    "parallelism": "replicas" if ws_world > 1 else "single GPU"},
         "roofline": roofline,
         "kernels": kernels,
@@ -701,124 +732,225 @@ def run_mxg(args, wl, ws_world, rank, local):
             "serial": {"value": round(job_tflops(flops, ws_world, e2e_ms), 2),
                        "ms_per_step": round(e2e_ms, 4),
                        "note": "copy in, compute, copy out, one step at a time"}},
-        "gpu_launches": int(launches),
-        "clocks": clk,
-        "wall_s_timed_region": round(t_wall, 4),
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+        "wall_s_timed_region": round(r["wall_s"], 4),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(wl, path.host)
+    del path
+
+    # ---- the other workloads of the same metric, one GPU only
+    extra = [c for c in args.configs.split(",") if c and c != wl.name]
+    if ws_world == 1 and extra:
+        from moe_grouped_block_gb300 import workloads
+        out = {}
+        for name in extra:
+            ewl = workloads.WORKLOADS[name]
+            epath = Path(ewl, args.out == "bf16", dev)
+            er = time_path(epath, args, min(args.steps, 20), None, dev, flush, stream)
+            ek, egn, egms = kernel_table(epath, ewl, er["per_kernel"], peaks)
+            eroof = gemm_roofline(egn, ewl.flops(), epath.kernel_bytes(egn), egms, peaks,
+                                  peak_src, ewl.fmt == "nvfp4", measured_traffic(ewl.name))
+            ems = float(np.mean(er["step_ms"]))
+            d = {"value": round(ewl.flops() / (ems * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                 "ms_per_step": round(ems, 5), "steps": len(er["step_ms"]),
+                 "config": {"G": ewl.G, "K": ewl.K, "N": ewl.N, "M": ewl.M, "mode": ewl.mode,
+                            "fmt": ewl.fmt, "step": " -> ".join(n for n, _ in er["stages"])},
+                 "roofline": eroof, "kernels": ek, "gpu_launches": er["launches"],
+                 "clocks": er["clocks"]}
+            if not args.no_cpu_baseline:
+                d["cpu_baseline"] = cpu_baseline(ewl, epath.host, full=True, single_core=False)
+            out[name] = d
+            del epath
+            torch.cuda.empty_cache()
+        line["configs"] = out
     if dist:
         dist.destroy_process_group()
     return line
 
 
 # ----------------------------------------------------------------------------- oracle timing
-def _oracle_sample(wl, rows_per_group: int, cols_per_group: int):
-    """One bounded sample of the workload through the oracle: quantize the
-    sampled activation rows and weight rows, then the fp64 GEMM on them.
-    Returns (seconds, algorithmic GEMM FLOP of the sample)."""
+# The oracle is timed on a fixed sample of the workload, the same in the
+# reference arm and in this arm's cpu_baseline: every expert's live rows and
+# the first eighth of its output columns (rounded up to 128), with the full
+# contraction.  A pass quantizes the sample's operands as the GPU step does
+# (offsets, activations / dY, weights) and runs the fp64 grouped GEMM.
+ORACLE_COL_FRAC = 1.0 / 8.0
+SINGLE_CORE_ROW_FRAC = 1.0 / 4.0  # the single-core figure takes a quarter of those rows
+
+
+def _ceil128(v: float) -> int:
+    return max(128, int(-(-int(np.ceil(v)) // 128)) * 128)
+
+
+def oracle_sample(wl, inp, row_frac: float = 1.0, col_frac: float = ORACLE_COL_FRAC):
+    """The sample's inputs: per expert the first ceil128(row_frac * M_g) of
+    its rows (at most M_g, rounded down to 128 for groups of any size) and the
+    first ceil128(col_frac * out) output columns.  Returns a dict of CPU
+    tensors with the sample's group sizes."""
     import torch
-    import oracle
-    from moe_grouped_block_gb300 import workloads
-    inp = workloads.make_inputs(wl) if not hasattr(wl, "_cached") else wl._cached
-    sizes = inp["sizes"].numpy()
     G, N, K = wl.G, wl.N, wl.K
-    flop = 0.0
-    t0 = time.perf_counter()
-    ws, _ = (oracle.group_offsets_unaligned if wl.sizes == "dirichlet_rows" else
-             oracle.group_offsets)(sizes, 1, K, wl.rows_capacity)
-    offs = oracle.live_rows(ws, G)
+    sizes = inp["sizes"].numpy().astype(np.int64)
+    if wl.sizes == "dirichlet_rows":  # timing only: whole 128-row blocks of each group
+        sizes = sizes // 128 * 128
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    rows = []
+    new_sizes = []
     for g in range(G):
-        lo, hi = int(offs[g]), int(offs[g + 1])
-        if hi == lo:
-            continue
-        r = min(rows_per_group, hi - lo)
-        r128 = max(128, (r + 127) // 128 * 128)
-        lo2 = min(lo, hi - r128) if hi - lo >= r128 else lo
-        c128 = max(128, min(N, (cols_per_group + 127) // 128 * 128))
-        if wl.mode == "fprop":
-            xs = inp["x"][lo2:lo2 + r128]
-            wsub = inp["w"][g, :c128]
-            if wl.fmt == "mxfp8":
-                qa = oracle.mxfp8_quantize(xs, r128, r128, rowwise=True, colwise=True)
-                qb = oracle.mxfp8_quantize(wsub, c128, c128)
-                a = {"q": qa["q_row"], "sf": qa["sf_row"]}
-                b = {"q": qb["q_row"], "sf": qb["sf_row"]}
-            else:
-                qa = oracle.nvfp4_quantize(xs, r128, r128)
-                qb = oracle.nvfp4_quantize(wsub, c128, c128)
-                a = {"q": qa["q_row"], "sf": qa["sf_row"], "outer": qa["outer_row"]}
-                b = {"q": qb["q_row"], "sf": qb["sf_row"], "outer": qb["outer_row"]}
-            oracle.grouped_gemm_fprop(wl.fmt, a, b, [0, r128], c128, K)
-            flop += 2.0 * r128 * c128 * K
-        elif wl.mode == "dgrad":
-            ds = inp["dy"][lo2:lo2 + r128]
-            wsub = inp["w"][g, :, :c128].contiguous()  # [N, c128]: the sample's K columns
-            qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=True)
-            qwt = oracle.mxfp8_quantize(wsub, N, N, rowwise=False, colwise=True)
-            oracle.grouped_gemm_dgrad({"q": qd["q_row"], "sf": qd["sf_row"]},
-                                      {"q": qwt["q_col"], "sf": qwt["sf_col"]}, [0, r128], 1,
-                                      N, c128)
-            flop += 2.0 * r128 * N * c128
+        r = min(int(sizes[g]), _ceil128(row_frac * sizes[g])) if sizes[g] else 0
+        r = r // 128 * 128
+        rows.append(np.arange(offs[g], offs[g] + r))
+        new_sizes.append(r)
+    rows = np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, np.int64)
+    rsel = torch.from_numpy(rows)
+    out = {"sizes": np.asarray(new_sizes, np.int64)}
+    out_cols = K if wl.mode == "dgrad" else N
+    c = min(out_cols, _ceil128(col_frac * out_cols))
+    out["cols"] = c
+    if wl.mode == "fprop":
+        out["x"] = inp["x"][rsel].contiguous()
+        out["w"] = inp["w"][:, :c].contiguous()             # [G, c, K]
+    elif wl.mode == "wgrad":
+        out["x"] = inp["x"][rsel].contiguous()               # [m, K]
+        out["dy"] = inp["dy"][rsel][:, :c].contiguous()      # [m, c]
+    else:
+        out["dy"] = inp["dy"][rsel].contiguous()             # [m, N]
+        out["w"] = inp["w"][:, :, :c].contiguous()           # [G, N, c]
+    return out
+
+
+def oracle_pass(wl, smp):
+    """One pass of the path through the oracle on a sample from
+    oracle_sample.  Returns (seconds, algorithmic GEMM FLOP of the sample)."""
+    import oracle
+    G, N, K = wl.G, wl.N, wl.K
+    sizes, c = smp["sizes"], smp["cols"]
+    m = int(sizes.sum())
+    t0 = time.perf_counter()
+    ws, _ = oracle.group_offsets(sizes, 1, K if wl.mode != "dgrad" else N, max(m, 128))
+    offs = oracle.live_rows(ws, G)
+    if m == 0:
+        return time.perf_counter() - t0, 0.0
+    if wl.mode == "fprop":
+        wq = smp["w"].reshape(G * c, K)
+        if wl.fmt == "mxfp8":
+            qa = oracle.mxfp8_quantize(smp["x"], m, m, rowwise=True, colwise=True)
+            qb = oracle.mxfp8_quantize(wq, G * c, G * c)
+            a = {"q": qa["q_row"], "sf": qa["sf_row"]}
+            b = {"q": qb["q_row"], "sf": qb["sf_row"]}
         else:
-            xs = inp["x"][lo2:lo2 + r128]
-            ds = inp["dy"][lo2:lo2 + r128, :c128].contiguous()
-            kk = min(K, c128)
-            if wl.fmt == "mxfp8":
-                qx = oracle.mxfp8_quantize(xs, r128, r128, rowwise=False, colwise=True)
-                qd = oracle.mxfp8_quantize(ds, r128, r128, rowwise=False, colwise=True)
-                a = {"q": qd["q_col"], "sf": qd["sf_col"]}
-                b = {"q": qx["q_col"], "sf": qx["sf_col"]}
-            else:
-                qx = oracle.nvfp4_quantize_colwise(xs, [0, r128], r128)
-                qd = oracle.nvfp4_quantize_colwise(ds, [0, r128], r128)
-                a = {"q": qd["q_col"], "sf": qd["sf_col"], "outer": qd["outer_col"]}
-                b = {"q": qx["q_col"], "sf": qx["sf_col"], "outer": qx["outer_col"]}
-            oracle.grouped_gemm_wgrad(a, b, [0, r128], r128, c128, K, sample_k=np.arange(kk),
-                                      fmt=wl.fmt)
-            flop += 2.0 * r128 * c128 * kk
+            qa = oracle.nvfp4_quantize(smp["x"], m, m)
+            qb = oracle.nvfp4_quantize(wq, G * c, G * c)
+            a = {"q": qa["q_row"], "sf": qa["sf_row"], "outer": qa["outer_row"]}
+            b = {"q": qb["q_row"], "sf": qb["sf_row"], "outer": qb["outer_row"]}
+        oracle.grouped_gemm_fprop(wl.fmt, a, b, offs, c, K)
+        flop = 2.0 * m * c * K
+    elif wl.mode == "wgrad":
+        if wl.fmt == "mxfp8":
+            qx = oracle.mxfp8_quantize(smp["x"], m, m, rowwise=False, colwise=True)
+            qd = oracle.mxfp8_quantize(smp["dy"], m, m, rowwise=False, colwise=True)
+            a = {"q": qd["q_col"], "sf": qd["sf_col"]}
+            b = {"q": qx["q_col"], "sf": qx["sf_col"]}
+        else:
+            qx = oracle.nvfp4_quantize_colwise(smp["x"], offs, m)
+            qd = oracle.nvfp4_quantize_colwise(smp["dy"], offs, m)
+            a = {"q": qd["q_col"], "sf": qd["sf_col"], "outer": qd["outer_col"]}
+            b = {"q": qx["q_col"], "sf": qx["sf_col"], "outer": qx["outer_col"]}
+        oracle.grouped_gemm_wgrad(a, b, offs, m, c, K, fmt=wl.fmt)
+        flop = 2.0 * m * c * K
+    else:
+        qd = oracle.mxfp8_quantize(smp["dy"], m, m, rowwise=True)
+        wq = smp["w"].reshape(G * N, c)
+        qwt = oracle.mxfp8_quantize(wq, G * N, G * N, rowwise=False, colwise=True)
+        oracle.grouped_gemm_dgrad({"q": qd["q_row"], "sf": qd["sf_row"]},
+                                  {"q": qwt["q_col"], "sf": qwt["sf_col"]}, offs, G, N, c)
+        flop = 2.0 * m * N * c
     return time.perf_counter() - t0, flop
 
 
-def _size_sample(wl, budget_s: float):
-    """Grow the per-expert sample (rows = weight rows = side) by doubling
-    until one sample takes at least a quarter of the budget."""
-    side = 128
-    t, f = _oracle_sample(wl, side, side)
-    while t < budget_s / 4 and side < max(wl.N, wl.K):
-        side *= 2
-        t, f = _oracle_sample(wl, side, side)
-    return side, t, f
+def _sample_text(wl, smp, row_frac):
+    out_cols = wl.K if wl.mode == "dgrad" else wl.N
+    rows = ("every live row of each expert" if row_frac >= 1 else
+            "the first %g of each expert's live rows" % row_frac)
+    return ("%s x the first %d of %d output columns, full contraction: offsets, "
+            "quantize of both operands and the fp64 grouped GEMM (%d sample rows)"
+            % (rows, smp["cols"], out_cols, int(smp["sizes"].sum())))
 
 
-def cpu_baseline(wl, budget_s: float = 15.0):
+def _single_core_main(path: str) -> None:
+    """Child process of the single-core timing: the sample is read from
+    `path` (saved by single_core_pass) and run with one thread."""
+    import torch
+    from moe_grouped_block_gb300 import workloads
+    d = torch.load(path, weights_only=False)
+    wl = workloads.WORKLOADS[d["workload"]]
+    t, f = oracle_pass(wl, d["sample"])
+    print(json.dumps({"seconds": t, "flop": f}))
+
+
+def single_core_pass(wl, smp):
+    """The oracle pass on `smp` in a child process limited to one thread
+    (OpenMP and BLAS).  Returns (seconds, FLOP) or None if it failed."""
+    import tempfile
+    import torch
+    with tempfile.TemporaryDirectory() as d:
+        f = os.path.join(d, "sample.pt")
+        torch.save({"workload": wl.name, "sample": smp}, f)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+                   MKL_NUM_THREADS="1", OMP_DYNAMIC="false")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-core", f],
+                           env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return None
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return out["seconds"], out["flop"]
+
+
+def cpu_baseline(wl, inp, full: bool = True, single_core: bool = True):
+    """The oracle on the host cores: the shared sample (the line's value), the
+    whole workload once (full), and a quarter of the sample's rows on one
+    thread (single_core)."""
     import oracle
     oracle.build()
-    side, t, f = _size_sample(wl, budget_s)
-    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": round(t, 2),
-            "sample": "per expert: up to %d activation rows x %d weight rows (full K=%d): "
-                      "MXFP8/NVFP4 quantize of both operands + fp64 GEMM; throughput = "
-                      "2*rows*cols*K of the sample / its time" % (side, min(side, wl.N), wl.K)}
+    smp = oracle_sample(wl, inp)
+    oracle_pass(wl, smp)  # first touch of the libraries
+    t, f = oracle_pass(wl, smp)
+    out = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+           "kind": "oracle", "seconds": round(t, 3), "sample": _sample_text(wl, smp, 1.0),
+           "same_sample_as": "bench.py --impl reference (one step)"}
+    if full:
+        fs = oracle_sample(wl, inp, 1.0, 1.0)
+        tf, ff = oracle_pass(wl, fs)
+        out["full"] = {"value": round(ff / tf / 1e12, 6), "seconds": round(tf, 3),
+                       "sample": "the whole workload: " + _sample_text(wl, fs, 1.0)}
+    if single_core:
+        s1 = oracle_sample(wl, inp, SINGLE_CORE_ROW_FRAC)
+        r = single_core_pass(wl, s1)
+        if r is not None:
+            out["single_core"] = {"value": round(r[1] / r[0] / 1e12, 6), "cores": 1,
+                                  "seconds": round(r[0], 3),
+                                  "sample": _sample_text(wl, s1, SINGLE_CORE_ROW_FRAC)}
+    return out
 
 
 def run_reference(args, wl, ws_world, rank):
     if rank != 0:
         return None
     import oracle
+    from moe_grouped_block_gb300 import workloads
     oracle.build()
-    # each step is a bounded sample; the whole run stays within a few minutes
-    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    side, _, _ = _size_sample(wl, per_step_budget)
+    inp = workloads.make_inputs(wl)
+    smp = oracle_sample(wl, inp)  # the sample the other arm's cpu_baseline times
     for _ in range(args.warmup):
-        _oracle_sample(wl, side, side)
+        oracle_pass(wl, smp)
     times, flops = [], []
     for _ in range(args.steps):
-        t, f = _oracle_sample(wl, side, side)
+        t, f = oracle_pass(wl, smp)
         times.append(t)
         flops.append(f)
     value = sum(flops) / sum(times) / 1e12
-    sample = "per expert: %d activation rows x %d weight rows, full K=%d" % (side, side, wl.K)
+    sample = _sample_text(wl, smp, 1.0)
     return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws_world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * float(np.mean(times)), 3), "higher_is_better": True,
@@ -842,7 +974,6 @@ def main():
     ap.add_argument("--out", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--epilogue", default="none", choices=["none", "bias_alpha"],
                     help="fprop: per-group bias and alpha in the GEMM epilogue")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-graph", action="store_true",
@@ -850,7 +981,13 @@ def main():
     ap.add_argument("--M", type=int, default=0, help="override live rows (profiling runs)")
     ap.add_argument("--N", type=int, default=0, help="override N (profiling runs)")
     ap.add_argument("--K", type=int, default=0, help="override K (profiling runs)")
+    ap.add_argument("--configs", default=",".join(EXTRA_CONFIGS),
+                    help="other workloads measured after the headline one (1 GPU; '' for none)")
+    ap.add_argument("--oracle-single-core", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_single_core:
+        _single_core_main(args.oracle_single_core)
+        return
     if args.warmup < 3 and args.impl == "mxg":
         args.warmup = 3
     from moe_grouped_block_gb300 import workloads

@@ -2,7 +2,8 @@
 whichever roofline time is larger, FLOP at the dense tensor peak or
 algorithmic bytes at the measured HBM bandwidth, and frac is the achieved
 fraction of that peak, equal to t_roofline / t; the measured DRAM traffic is
-reported only while the GEMM sources hash to the digest it was taken on; the
+reported only while the GEMM sources and compile flags hash to the digest it
+was taken on; the oracle timing sample is the same in both arms; the
 clock record's throttle reasons are read from nvidia-smi lines or NVML bits."""
 import os
 import sys
@@ -54,35 +55,24 @@ def test_finegrained_sits_just_on_the_tensor_side():
     assert r["t_tensor_roofline_ms"] > r["t_hbm_roofline_ms"]
 
 
-ROW = "| mixtral_fprop_mxfp8 | `k` | 568991744 | 446700800 | 1015692544 | 620.7 | alg |\n"
+def test_traffic_is_reported_only_for_the_measured_sources():
+    fresh = {"digest": bench.gemm_source_digest(),
+             "bytes": {"mixtral_fprop_mxfp8": 1015692544, "wgrad_mxfp8": 30}}
+    assert bench.measured_traffic("mixtral_fprop_mxfp8", fresh) == 1015692544
+    assert bench.measured_traffic("wgrad_mxfp8", fresh) == 30
+    assert bench.measured_traffic("no_such_workload", fresh) is None
+    # the same table measured on other sources or flags (the kernel changed since): none
+    stale = dict(fresh, digest="0" * 64)
+    assert bench.measured_traffic("mixtral_fprop_mxfp8", stale) is None
+    # no table at all: none
+    assert bench.measured_traffic("mixtral_fprop_mxfp8", {"digest": None, "bytes": {}}) is None
 
 
-def test_traffic_is_reported_only_for_the_measured_sources(tmp_path, monkeypatch):
-    head = "| workload | kernel | read bytes | write bytes | traffic bytes | us | alg |\n|---|---|---|---|---|---|---|\n"
-    fresh = tmp_path / "fresh.md"
-    fresh.write_text("sources sha256: `%s`\n\n" % bench.gemm_source_digest() + head + ROW)
-    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(fresh))
-    assert bench.measured_traffic("mixtral_fprop_mxfp8") == 1015692544
-    assert bench.measured_traffic("no_such_workload") is None
-    # the same table measured on other sources (the kernel changed since): none
-    stale = tmp_path / "stale.md"
-    stale.write_text("sources sha256: `%s`\n\n" % ("0" * 64) + head + ROW)
-    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(stale))
-    assert bench.measured_traffic("mixtral_fprop_mxfp8") is None
-    # no summary at all: none
-    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(tmp_path / "absent.md"))
-    assert bench.measured_traffic("mixtral_fprop_mxfp8") is None
-
-
-def test_traffic_table_row_is_read_by_workload(tmp_path, monkeypatch):
-    digest = bench.gemm_source_digest()
-    table = ("sources sha256: `%s`\n\n| workload | kernel | read bytes | write bytes | traffic bytes |\n"
-             "|---|---|---|---|---|\n| wl_a | `k` | 1 | 2 | 3 |\n| wl_b | `k` | 10 | 20 | 30 |\n" % digest)
-    f = tmp_path / "traffic.md"
-    f.write_text(table)
-    monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(f))
-    assert bench.measured_traffic("wl_a") == 3
-    assert bench.measured_traffic("wl_b") == 30
+def test_digest_covers_the_compile_flags(monkeypatch):
+    from moe_grouped_block_gb300 import build as mxg_build
+    d0 = bench.gemm_source_digest()
+    monkeypatch.setattr(mxg_build, "NVCC_FLAGS", mxg_build.NVCC_FLAGS + ["-maxrregcount=128"])
+    assert bench.gemm_source_digest() != d0
 
 
 def test_digest_ignores_comments_but_not_code():
@@ -129,3 +119,32 @@ def test_clock_reasons_from_nvml_samples():
     assert r["sm_mhz"] == 2070 and r["sm_max_mhz"] == 2070 and r["samples"] == 4
     # 0x1 (idle) is not a throttle reason; 0x4 power cap, 0x40 hardware thermal
     assert r["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_oracle_sample_covers_every_expert_and_an_eighth_of_the_columns():
+    """The oracle's timing sample: every live row of each expert and the first
+    eighth of the output columns (rounded up to 128); FLOP = 2 m c K."""
+    from moe_grouped_block_gb300 import workloads
+    wl = workloads.WORKLOADS["tiny_fprop_mxfp8"].scaled(N=1024)
+    inp = workloads.make_inputs(wl)
+    smp = bench.oracle_sample(wl, inp)
+    assert list(smp["sizes"]) == [128, 0, 256, 128] and smp["cols"] == 128
+    assert tuple(smp["x"].shape) == (512, wl.K) and tuple(smp["w"].shape) == (wl.G, 128, wl.K)
+    quarter = bench.oracle_sample(wl, inp, 0.25)
+    assert list(quarter["sizes"]) == [128, 0, 128, 128]
+    t, f = bench.oracle_pass(wl, smp)
+    assert f == 2.0 * 512 * 128 * wl.K and t > 0
+    for name in ("wgrad_mxfp8", "dgrad_mxfp8", "rowscaled_fprop_nvfp4", "wgrad_nvfp4"):
+        w2 = workloads.WORKLOADS[name].scaled(M=512, K=256, N=256, G=2, sizes="fixed",
+                                              fixed_sizes=(384, 128))
+        s2 = bench.oracle_sample(w2, workloads.make_inputs(w2))
+        t2, f2 = bench.oracle_pass(w2, s2)
+        assert f2 == 2.0 * 512 * 128 * 256, name
+
+
+def test_single_core_child_runs_the_same_pass():
+    from moe_grouped_block_gb300 import workloads
+    wl = workloads.WORKLOADS["tiny_fprop_mxfp8"]
+    smp = bench.oracle_sample(wl, workloads.make_inputs(wl))
+    r = bench.single_core_pass(wl, smp)
+    assert r is not None and r[1] == bench.oracle_pass(wl, smp)[1]
