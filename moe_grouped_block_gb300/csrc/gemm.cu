@@ -64,6 +64,7 @@ struct GemmParams {
   int out_bf16;
   int inject;  // test hook: bit 0 withholds the first accumulator-ready arrival of CTA 0
   int c_align32;  // C is 32-byte aligned (whole-sector epilogue stores)
+  int vec_col;    // bias and the NVFP4 column outer scales are 16-byte aligned
   int unaligned;  // group sizes of any value (MXFP8, CTA-pair kernel only)
 };
 
@@ -115,6 +116,8 @@ struct TileInfo {
   int64_t a_kb0, b_kb0;      // first K block of A and of B
   int64_t c_row, c_col;      // top-left output element
   int64_t row_end;           // rows of C at or beyond this are not written
+  bool half_n;               // CTA-pair unit whose last 128 output columns are past the
+                             // output width: its MMAs run with N = 128
 };
 
 // Work unit t of the single-CTA kernel -> one 128 x BN output tile.
@@ -164,6 +167,7 @@ __device__ __forceinline__ TileInfo map_tile(int64_t t, const GemmParams& p, con
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
   }
   ti.a_sf_row = ti.a_row;
+  ti.half_n = false;
   return ti;
 }
 
@@ -244,77 +248,98 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
   if (lane == 0 && blockIdx.x == 0) status_set(p.status, bits);
 }
 
+// Four consecutive fp32 values at p (16-byte aligned when vec, else any
+// 4-byte alignment).  Callers pass addresses that are the same for every
+// lane of the warp, so each load is a single broadcast transaction.
+__device__ __forceinline__ float4 load4(const float* p, bool vec) {
+  if (vec) return *reinterpret_cast<const float4*>(p);
+  return make_float4(p[0], p[1], p[2], p[3]);
+}
+
 // One output row of the epilogue: 128 accumulator columns (v, four loads of
-// 32) starting at column c_col + col0, with alpha, the NVFP4 outer scales,
-// bias and beta applied, stored as fp32 or bf16.  Rows at or beyond the
+// 32) starting at column c_col + col0, turned into
+//   alpha_g * acc [* outer_row * outer_col (NVFP4)] [+ bias] [+ beta_g * C]
+// and stored as fp32 or bf16 (round to nearest even).  Rows at or beyond the
 // tile's row_end, and the upper half of a half-wide last column unit, are
-// skipped.  Each thread owns a row, so a store instruction
-// touches 32 rows: with a 32-byte-aligned C every store fills whole 32-byte
-// sectors (16 bf16 or 8 fp32 per store), else 16-byte stores are used.
+// skipped.  Each thread owns a row, so a store instruction touches 32 rows:
+// with a 32-byte-aligned C every store fills whole 32-byte sectors (16 bf16
+// or 8 fp32 per store), else 16-byte stores are used.  The column operands
+// (NVFP4 column outer scales, bias) are the same for all lanes and are read
+// four at a time; beta and bias checks are made once per row, not per element.
 template <bool NVF4>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
-                                             uint32_t col0, const uint32_t (&v)[4][32],
-                                             bool has_k) {
+                                             uint32_t col0, uint32_t (&v)[4][32], bool has_k) {
   if (row >= ti.row_end || ti.c_col + col0 >= p.out_cols) return;
   const int64_t cbase = row * p.out_cols + ti.c_col + col0;
   const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
   const float beta = p.beta ? p.beta[ti.g] : 0.0f;
-  float rs = 1.0f;
-  const float* cs = nullptr;
   const float* bs =
       p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0 : nullptr;
+  float rs = 1.0f;
+  const float* cs = nullptr;
   if (NVF4) {  // fprop: per-row / per-weight-row; wgrad: per (group, column) of dY / X
     rs = p.a_outer[row];
     cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
   }
-  // value of accumulator column j = 32c + e after alpha, outer scales and bias
-  auto value = [&](int c, int e) {
-    const int j = 32 * c + e;
-    float a = has_k ? __uint_as_float(v[c][e]) : 0.0f;
-    if (NVF4) a = a * rs * cs[j];
-    float o = alpha * a;
-    if (bs) o += bs[j];
-    return o;
-  };
-  if (p.out_bf16) {
-    uint16_t* out = static_cast<uint16_t*>(p.C) + cbase;
+  // 16 columns at a time (32 bytes of bf16 or 64 of fp32), transformed in
+  // place in the accumulator registers
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+  for (int k = 0; k < 8; ++k) {
+    uint32_t* a = &v[k >> 1][16 * (k & 1)];
+    const int j0 = 16 * k;  // first column of the 16
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // 16 columns = 32 bytes
-        uint16_t* dst = out + 32 * c + 16 * h;
-        uint32_t w[8];
+    for (int e = 0; e < 16; e += 4) {
+      float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f), b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (NVF4) s4 = load4(cs + j0 + e, p.vec_col);
+      if (bs) b4 = load4(bs + j0 + e, p.vec_col);
+      const float sc[4] = {s4.x, s4.y, s4.z, s4.w}, bi[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float o0 = value(c, 16 * h + 2 * q), o1 = value(c, 16 * h + 2 * q + 1);
-          if (beta != 0.0f) {
-            const uint32_t old = reinterpret_cast<const uint32_t*>(dst)[q];
-            o0 += beta * bf16lo(old);
-            o1 += beta * bf16hi(old);
-          }
-          w[q] = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
-        }
-        if (p.c_align32) {
-          st_global_32B(dst, w);
-        } else {
-          reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
+      for (int i = 0; i < 4; ++i) {
+        float x = has_k ? __uint_as_float(a[e + i]) : 0.0f;
+        if (NVF4) x = x * rs * sc[i];
+        x *= alpha;
+        if (bs) x += bi[i];
+        a[e + i] = __float_as_uint(x);
       }
     }
-  } else {
-    float* out = static_cast<float*>(p.C) + cbase;
+    if (p.out_bf16) {
+      uint16_t* dst = static_cast<uint16_t*>(p.C) + cbase + j0;
+      uint32_t w[8];
+      if (beta != 0.0f) {
+        const uint4 q0 = reinterpret_cast<const uint4*>(dst)[0];
+        const uint4 q1 = reinterpret_cast<const uint4*>(dst)[1];
+        const uint32_t old[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+        for (int q = 0; q < 8; ++q)
+          w[q] = cvt_bf16x2(__uint_as_float(a[2 * q]) + beta * bf16lo(old[q]),
+                            __uint_as_float(a[2 * q + 1]) + beta * bf16hi(old[q]));
+      } else {
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {  // 8 columns = 32 bytes
-        float* dst = out + 32 * c + 8 * h;
+        for (int q = 0; q < 8; ++q)
+          w[q] = cvt_bf16x2(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1]));
+      }
+      if (p.c_align32) {
+        st_global_32B(dst, w);
+      } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    } else {
+      float* out = static_cast<float*>(p.C) + cbase + j0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // 8 columns = 32 bytes
+        float* dst = out + 8 * h;
         uint32_t w[8];
+        if (beta != 0.0f) {
+          const float4 q0 = reinterpret_cast<const float4*>(dst)[0];
+          const float4 q1 = reinterpret_cast<const float4*>(dst)[1];
+          const float old[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float o = value(c, 8 * h + q);
-          if (beta != 0.0f) o += beta * dst[q];
-          w[q] = __float_as_uint(o);
+          for (int q = 0; q < 8; ++q)
+            w[q] = __float_as_uint(__uint_as_float(a[8 * h + q]) + beta * old[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) w[q] = a[8 * h + q];
         }
         if (p.c_align32) {
           st_global_32B(dst, w);
@@ -600,16 +625,20 @@ struct PairCfg {
   static constexpr uint32_t kIdesc = (NVF4 ? ((1u << 7) | (1u << 10)) : 0u) |
                                      (static_cast<uint32_t>(BN >> 3) << 17) |
                                      (NVF4 ? 0u : (1u << 23)) | ((256u >> 4) << 24);
+  // the same with N = 128, for a half-wide last column unit: each CTA then
+  // supplies 64 rows of B (the first 64 of its tile)
+  static constexpr uint32_t kIdescN128 = (kIdesc & ~(0x3Fu << 17)) | ((128u >> 3) << 17);
 };
 
 // Work unit t -> this CTA's half.  fprop / dgrad: 256 rows of one group (the
 // upper half may run past the group's end: it is computed but not stored)
 // times 256 output columns.  wgrad: 256 rows of dW_g times 256 columns.
 // When the output width is an odd multiple of 128 the last column unit is
-// half wide: its upper 128 B rows are loaded (another group's rows, or the
-// zero fill past the tensor's end) but those columns are not stored.
+// half wide (half_n): its MMAs run with N = 128, for which each CTA supplies
+// 64 rows of B, so CTA r loads its B tile from b_row + 64 r (the tile's last
+// 64 rows are loaded but not read).
 // a_row is this CTA's first A row; b_row is the unit's first B row (this CTA
-// loads b_row + 128 * rank).  Row units and the wgrad contraction are counted
+// loads b_row + 128 * rank, or b_row + 64 * rank when half wide).  Row units and the wgrad contraction are counted
 // on the padded offsets, so unaligned groups (a last 128-row tile partly past
 // the group) need nothing else: A's data rows start at the group's row
 // offset, its scale rows (a_sf_row) and its colwise slabs at the padded one.
@@ -656,6 +685,7 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
   }
+  ti.half_n = ti.c_col + 256 > p.out_cols;
   return ti;
 }
 
@@ -734,7 +764,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
       bool ok = true;
       for (int64_t t = unit0; ok && t < total_units; t += ustride) {
         const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
-        const int32_t b_half = static_cast<int32_t>(ti.b_row + 128 * rank);
+        // this CTA's half of B: rows 128r.. of the unit, or 64r.. when the
+        // unit is half wide and its MMAs run with N = 128
+        const int32_t b_half = static_cast<int32_t>(ti.b_row + (ti.half_n ? 64 : 128) * rank);
         const int32_t a_band = static_cast<int32_t>(ti.a_sf_row >> 7);
         const int32_t b_band = static_cast<int32_t>(ti.b_row >> 7);
         for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
@@ -807,6 +839,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
           const uint32_t sb = sa + Cfg::kATile;
           const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
+          const uint32_t idesc = ti.half_n ? Cfg::kIdescN128 : Cfg::kIdesc;
 #pragma unroll
           for (int kk = 0; kk < Cfg::kMmas; ++kk) {
             // K step kk: sub-tile kk / kMmasPerSub, 32 bytes further along the
@@ -817,13 +850,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
             const uint64_t bdesc = smem_desc(sb + off, 16, 8 * Cfg::kSubK, Cfg::kSwizzle) + 2 * ks;
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (NVF4) {
-              tc_mma_nvf4_pair(tmem_base, adesc, bdesc, Cfg::kIdesc, sfa_t + 4 * kk,
-                               sfb_t + 8 * kk, accum);
+              tc_mma_nvf4_pair(tmem_base, adesc, bdesc, idesc, sfa_t + 4 * kk, sfb_t + 8 * kk,
+                               accum);
             } else {
               // scale tile kk / 4 (A at 4 columns per tile, B's two bands at 8),
               // byte kk % 4 of its 32-bit columns
               const uint32_t sid = static_cast<uint32_t>(kk & 3), atom = static_cast<uint32_t>(kk >> 2);
-              tc_mma_mxf8_pair(tmem_base, adesc, bdesc, Cfg::kIdesc | (sid << 4) | (sid << 29),
+              tc_mma_mxf8_pair(tmem_base, adesc, bdesc, idesc | (sid << 4) | (sid << 29),
                                sfa_t + 4 * atom, sfb_t + 8 * atom, accum);
             }
           }
@@ -1031,6 +1064,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.bias = bias;
   p.C = C;
   p.c_align32 = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 ? 1 : 0;
+  p.vec_col = ((reinterpret_cast<uintptr_t>(b_outer) | reinterpret_cast<uintptr_t>(bias)) & 15u) == 0
+                  ? 1 : 0;
   p.status = status;
   p.M_cap = M_cap;
   p.N = N;
