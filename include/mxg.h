@@ -23,7 +23,9 @@
  *     (int32, atomicOr of the MXG_DEV_* bits) and clamp so that no access
  *     leaves the buffers.  Read it after the stream or graph has completed.
  *     `dev_status` may be NULL (then nothing is recorded).
- *   - Rows are dense: a [rows, cols] matrix has leading dimension cols.
+ *   - Rows are dense (a [rows, cols] matrix has leading dimension cols),
+ *     except the GEMM operands' data, whose leading dimension the operand
+ *     descriptor gives.
  *   - bf16 is IEEE bfloat16 stored as uint16; E4M3 is the "fn" variant.
  *   - The grouped matrices are 128-row aligned: every group size, K, N and
  *     rows_capacity is a multiple of 128 (the alignment [PR2763] states for
@@ -80,19 +82,33 @@ typedef enum {
 
 typedef enum { MXG_OUT_F32 = 0, MXG_OUT_BF16 = 1 } mxg_out_t;
 
-/* One quantized GEMM operand: rowwise-quantized rows of the contraction dim.
- *   data  : E4M3 bytes [rows, kdim] (MXFP8) or packed E2M1 [rows, kdim/2]
- *           (NVFP4, element 2i in the low nibble of byte i).
+/* One quantized GEMM operand: rowwise-quantized rows of the contraction dim
+ * ([PR2763] GEMM-setup review thread: per-group operand pointers come from
+ * the offsets and the leading dimensions).
+ *   data  : E4M3 bytes [rows, cols] (MXFP8) or packed E2M1 [rows, cols/2]
+ *           (NVFP4, element 2i in the low nibble of byte i), consecutive rows
+ *           ld elements apart.
  *   scale : block scales in the swizzled layout of [TE-gemm] swizzled_scale
- *           for the [rows, kdim/32] (MXFP8) or [rows, kdim/16] (NVFP4) scale
+ *           for the [rows, cols/32] (MXFP8) or [rows, cols/16] (NVFP4) scale
  *           matrix: 128x4 tiles of 512 contiguous bytes, byte
  *           ((r/128 * C/4 + c/4) * 32 + r%32) * 16 + (r%128)/32 * 4 + c%4.
+ *           Always dense (the swizzle fixes its layout).
  *   outer : NVFP4 only: FP32 outer scale per row [rows]; NULL for MXFP8.
+ *   rows, cols : the operand's rows and contraction length in elements, as
+ *           the GEMM mode implies them (listed at mxg_grouped_gemm); 0 means
+ *           "as implied" (no check), any other value must match.
+ *   ld    : elements from one row of data to the next; 0 means cols (dense).
+ *           Otherwise ld >= cols and ld bytes (ld for MXFP8, ld/2 for NVFP4,
+ *           ld even) a multiple of 16, so that an operand can be a view of
+ *           rows inside a wider buffer.
  * data and scale must be 16-byte aligned. */
 typedef struct {
   const void* data;
   const uint8_t* scale;
   const float* outer;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
 } mxg_operand_t;
 
 /* ------------------------------------------------------------------------- */
@@ -216,9 +232,14 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *             may be NULL.
  * Accumulation is FP32 in tensor memory; the FP32 output is the parity
  * output, bf16 is rounded to nearest even from it.
+ * Operand shapes (rows x cols of mxg_operand_t, checked when nonzero):
+ *   FPROP_TN: A M_cap x K, B G*N x K;  WGRAD_NT: A N x M_cap, B K x M_cap;
+ *   DGRAD_NN: A M_cap x N, B K x G*N.
  * Errors: INVALID_ARG (nulls, G < 1 or G > 1024, NVFP4 dgrad, beta with
- * NVFP4 -- rejected as on [PR3661]), ALIGNMENT (M_cap, N, K not multiples of
- * 128; data/scale/C not 16-byte aligned), UNSUPPORTED_ARCH, LAUNCH. */
+ * NVFP4 -- rejected as on [PR3661] --, an operand's rows or cols not the
+ * mode's, ld < cols), ALIGNMENT (M_cap, N, K not multiples of 128;
+ * data/scale/C not 16-byte aligned; ld bytes not a multiple of 16),
+ * UNSUPPORTED_ARCH, LAUNCH. */
 mxg_status_t mxg_grouped_gemm(mxg_format_t fmt, mxg_gemm_mode_t mode, const mxg_operand_t* A,
                               const mxg_operand_t* B, const int64_t* group_ws, int G,
                               int64_t M_cap, int64_t N, int64_t K, const float* alpha,
@@ -315,7 +336,8 @@ mxg_status_t mxg_group_quantize_unaligned(mxg_qlayout_t layout, const void* x,
  *   WGRAD_NT : A = dY colwise [N, R_pad] + [N, R_pad/32], B = X colwise
  *              [K, R_pad] + [K, R_pad/32]; each group contracts over its
  *              padded slab (the zero padding adds nothing);
- *   DGRAD_NN : A data [M_cap, N] dense, A scale [R_pad, N/32] padded.
+ *   DGRAD_NN : A data [M_cap, N] dense, A scale [R_pad, N/32] padded
+ *              (WGRAD_NT operands are R_pad columns long).
  * Output rows are the dense data rows; rows past a group are not written.
  * Errors: as mxg_grouped_gemm, plus INVALID_ARG when B has fewer than 256
  * rows (G * N for fprop, K otherwise) or M_cap + 128 * G exceeds 2^31 - 128. */

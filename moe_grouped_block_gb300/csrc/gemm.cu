@@ -632,7 +632,7 @@ struct PairCfg {
 
 // Work unit t -> this CTA's half.  fprop / dgrad: 256 rows of one group (the
 // upper half may run past the group's end: it is computed but not stored)
-// times 256 output columns.  wgrad: 256 rows of dW_g times 256 columns.
+// times 256 output columns, walked group-major.  wgrad: 256 rows of dW_g times 256 columns.
 // When the output width is an odd multiple of 128 the last column unit is
 // half wide (half_n): its MMAs run with N = 128, for which each CTA supplies
 // 64 rows of B, so CTA r loads its B tile from b_row + 64 r (the tile's last
@@ -659,7 +659,15 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     const int g = lo;
     const int64_t mu = (((prow_off[g + 1] - prow_off[g]) >> 7) + 1) >> 1;
     const int64_t local = t - tile_off[g];
-    const int64_t n_tile = local / mu, mu_i = local % mu;
+    // fprop: column unit, then row unit (the clusters in flight share one
+    // weight tile and the expert's activation rows stay in L2).  dgrad: row
+    // unit, then column unit: its contraction runs over the FFN width, so an
+    // expert's dY rows (up to tens of MB) are read by every column unit; with
+    // the columns innermost a wave reads a few row units' dY once and keeps the
+    // expert's transposed weight slab in L2 for the next wave
+    const int64_t ncu = (p.out_cols + 255) >> 8;
+    const int64_t n_tile = p.mode == 2 ? local % ncu : local / mu;
+    const int64_t mu_i = p.mode == 2 ? local / ncu : local % mu;
     ti.g = g;
     ti.a_row = row_off[g] + 256 * mu_i + 128 * rank;
     ti.a_sf_row = prow_off[g] + 256 * mu_i + 128 * rank;
@@ -968,13 +976,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
 // ---------------------------------------------------------------- host side
 namespace {
 
-// 2-D byte tensor [rows, inner_bytes], box [box_rows, bk bytes], with the
-// swizzle of the same width (the layout the K-major MMA descriptors above
-// describe).
+// 2-D byte tensor [rows, inner_bytes] with rows row_bytes apart, box
+// [box_rows, bk bytes], with the swizzle of the same width (the layout the
+// K-major MMA descriptors above describe).
 bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows,
-               uint32_t box_rows, int bk) {
+               uint64_t row_bytes, uint32_t box_rows, int bk) {
   const int box = bk > 128 ? 128 : bk;  // a 256-byte stage is loaded as two boxes
-  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner_bytes, rows, inner_bytes,
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, inner_bytes, rows, row_bytes,
                       static_cast<uint32_t>(box), box_rows,
                       box == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
@@ -1049,7 +1057,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
                                 int num_sms, int tile_n, int stage_bytes, int inject,
-                                uint64_t timeout_ns, int unaligned, cudaStream_t stream) {
+                                uint64_t timeout_ns, int unaligned, int64_t a_ld_bytes,
+                                int64_t b_ld_bytes, cudaStream_t stream) {
   GemmParams p;
   p.unaligned = unaligned;
   p.inject = inject;
@@ -1109,8 +1118,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
     const uint64_t sfb_strides[2] = {512, static_cast<uint64_t>(512 * p.b_atoms_row)};
     const uint32_t sfb_box[3] = {128, static_cast<uint32_t>(atoms), 2};
     const int64_t ebn = nvfp4 ? 1 : 2;  // bytes per element x 2
-    if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows, 128, BKB) ||
-        !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows, 128, BKB) ||
+    if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebn / 2), a_rows,
+                   static_cast<uint64_t>(a_ld_bytes), 128, BKB) ||
+        !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebn / 2), b_rows,
+                   static_cast<uint64_t>(b_ld_bytes), 128, BKB) ||
         !make_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a_sf, 128,
                       static_cast<uint64_t>((a_sf_rows / 128) * p.a_atoms_row), 512, 128,
                       static_cast<uint32_t>(atoms), CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -1131,8 +1142,10 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   const int bn = (tile_n == 128 || p.out_cols % 256 != 0) ? 128 : 256;
   const int64_t ebytes_num = nvfp4 ? 1 : 2;  // bytes per element x 2
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows, 128, BKB) ||
-      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows, bn, BKB))
+  if (!make_tmap(&ta, a_data, static_cast<uint64_t>(a_kdim * ebytes_num / 2), a_rows,
+                 static_cast<uint64_t>(a_ld_bytes), 128, BKB) ||
+      !make_tmap(&tb, b_data, static_cast<uint64_t>(b_kdim * ebytes_num / 2), b_rows,
+                 static_cast<uint64_t>(b_ld_bytes), bn, BKB))
     return cudaErrorInvalidValue;
   // upper bound on the work units (device-side group sizes are unknown here)
   const int64_t max_units = mode == 1 ? G * (N / 128) * (K / bn)

@@ -30,7 +30,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 int64_t N, int64_t K, const float* alpha, const float* beta,
                                 const float* bias, void* C, int out_bf16, int32_t* status,
                                 int num_sms, int tile_n, int stage_bytes, int inject,
-                                uint64_t timeout_ns, int unaligned, cudaStream_t stream);
+                                uint64_t timeout_ns, int unaligned, int64_t a_ld_bytes,
+                                int64_t b_ld_bytes, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -89,6 +90,21 @@ bool offsets_args_ok(const void* sizes, const int64_t* ws, int G, int64_t multip
   return sizes != nullptr && ws != nullptr && G >= 1 && G <= 65536 && multiplier >= 1 &&
          multiplier <= (1LL << 31) && last_dim >= 1 && rows_capacity >= 0 &&
          rows_capacity <= (1LL << 62) && rows_capacity <= INT64_MAX / last_dim;
+}
+
+// Checks an operand descriptor's rows / cols (0 = as the mode implies) and
+// leading dimension (0 = dense) and returns the data's row stride in bytes.
+mxg_status_t operand_shape(const mxg_operand_t* op, int64_t rows, int64_t cols, bool nvfp4,
+                           int64_t* ld_bytes) {
+  if ((op->rows != 0 && op->rows != rows) || (op->cols != 0 && op->cols != cols))
+    return MXG_ERR_INVALID_ARG;
+  const int64_t ld = op->ld == 0 ? cols : op->ld;
+  if (ld < cols) return MXG_ERR_INVALID_ARG;
+  if (nvfp4 && (ld & 1)) return MXG_ERR_ALIGNMENT;
+  const int64_t bytes = nvfp4 ? ld / 2 : ld;
+  if (bytes % 16 != 0) return MXG_ERR_ALIGNMENT;
+  *ld_bytes = bytes;
+  return MXG_OK;
 }
 
 }  // namespace
@@ -245,6 +261,17 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   if (!aligned16(A->data) || !aligned16(A->scale) || !aligned16(B->data) || !aligned16(B->scale) ||
       !aligned16(C))
     return MXG_ERR_ALIGNMENT;
+  // operand shapes the mode implies (rows x contraction elements) and the
+  // leading dimensions of the data, in bytes
+  const int64_t M_pad = M_cap + (unaligned ? 128 * static_cast<int64_t>(G) : 0);
+  const int64_t a_rows = mode == MXG_WGRAD_NT ? N : M_cap;
+  const int64_t a_cols = mode == MXG_FPROP_TN ? K : (mode == MXG_WGRAD_NT ? M_pad : N);
+  const int64_t b_rows = mode == MXG_FPROP_TN ? N * static_cast<int64_t>(G) : K;
+  const int64_t b_cols = mode == MXG_FPROP_TN ? K : (mode == MXG_WGRAD_NT ? M_pad : N * G);
+  int64_t a_ld = 0, b_ld = 0;
+  mxg_status_t sh = operand_shape(A, a_rows, a_cols, nv, &a_ld);
+  if (sh != MXG_OK) return sh;
+  if ((sh = operand_shape(B, b_rows, b_cols, nv, &b_ld)) != MXG_OK) return sh;
   int sms = 0;
   const mxg_status_t st = current_device(&sms);
   if (st != MXG_OK) return st;
@@ -253,7 +280,8 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
                       nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,
                       out_type == MXG_OUT_BF16 ? 1 : 0, dev_status, sms, tile_n, stage_bytes,
-                      inject, timeout_ns, unaligned, reinterpret_cast<cudaStream_t>(stream)),
+                      inject, timeout_ns, unaligned, a_ld, b_ld,
+                      reinterpret_cast<cudaStream_t>(stream)),
                   1);
 }
 

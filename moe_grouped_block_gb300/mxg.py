@@ -42,7 +42,20 @@ class MxgError(RuntimeError):
 
 class Operand(ctypes.Structure):
     """mxg_operand_t"""
-    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("outer", ctypes.c_void_p)]
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("outer", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld", ctypes.c_int64)]
+
+
+def _operand(T, elems_per_byte: int) -> Operand:
+    """(data, scale[, outer]) -> mxg_operand_t.  A 2-D data tensor passes its
+    leading dimension (row stride in elements), so a view of rows inside a
+    wider buffer is described as such; rows and cols are left to the library
+    (0: as the GEMM mode implies)."""
+    data = T[0]
+    ld = 0
+    if isinstance(data, torch.Tensor) and data.dim() == 2:
+        ld = data.stride(0) * elems_per_byte
+    return Operand(_p(data), _p(T[1]), _p(T[2]) if len(T) > 2 else None, 0, 0, ld)
 
 
 _lib = None
@@ -155,8 +168,8 @@ def mxg_grouped_gemm(fmt: int, mode: int, A: tuple, B: tuple, group_ws: torch.Te
                      out_type: int = MXG_OUT_F32, workspace=None, workspace_bytes: int = 0,
                      dev_status=None, stream=None, bias=None) -> None:
     """A, B: (data, scale, outer-or-None) device tensors."""
-    a = Operand(_p(A[0]), _p(A[1]), _p(A[2]) if len(A) > 2 else None)
-    b = Operand(_p(B[0]), _p(B[1]), _p(B[2]) if len(B) > 2 else None)
+    epb = 2 if fmt == MXG_NVFP4_ROWSCALED else 1
+    a, b = _operand(A, epb), _operand(B, epb)
     _check("mxg_grouped_gemm",
            load().mxg_grouped_gemm(fmt, mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws), G,
                                    M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C), out_type,
@@ -169,8 +182,8 @@ def mxg_grouped_gemm_debug(fmt: int, mode: int, A: tuple, B: tuple, group_ws, G:
                            out_type: int = MXG_OUT_F32, dev_status=None, tile_n: int = 0,
                            stage_bytes: int = 0, inject_flags: int = 0, wait_timeout_ns: int = 0,
                            stream=None, bias=None) -> None:
-    a = Operand(_p(A[0]), _p(A[1]), _p(A[2]) if len(A) > 2 else None)
-    b = Operand(_p(B[0]), _p(B[1]), _p(B[2]) if len(B) > 2 else None)
+    epb = 2 if fmt == MXG_NVFP4_ROWSCALED else 1
+    a, b = _operand(A, epb), _operand(B, epb)
     _check("mxg_grouped_gemm_debug",
            load().mxg_grouped_gemm_debug(fmt, mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws),
                                          G, M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C),
@@ -218,8 +231,7 @@ def mxg_grouped_gemm_unaligned(mode: int, A: tuple, B: tuple, group_ws: torch.Te
                                out_type: int = MXG_OUT_F32, dev_status=None, stream=None,
                                bias=None) -> None:
     """A, B: (data, scale) device tensors (MXFP8)."""
-    a = Operand(_p(A[0]), _p(A[1]), None)
-    b = Operand(_p(B[0]), _p(B[1]), None)
+    a, b = _operand(A[:2], 1), _operand(B[:2], 1)
     _check("mxg_grouped_gemm_unaligned",
            load().mxg_grouped_gemm_unaligned(mode, ctypes.byref(a), ctypes.byref(b), _p(group_ws),
                                              G, M_cap, N, K, _p(alpha), _p(beta), _p(bias), _p(C),

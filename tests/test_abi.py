@@ -124,6 +124,31 @@ def test_gemm_argument_errors(lib):
 
 
 @no_device_only
+def test_gemm_operand_descriptor_errors(lib):
+    """rows / cols other than the mode's, a leading dimension below cols or
+    not a multiple of 16 bytes: refused before any launch."""
+    r = ctypes.byref
+    g = lib.mxg_grouped_gemm
+    ok = mxg.Operand(FAKE, FAKE, None, 0, 0, 0)
+
+    def call(a, b, fmt=1, mode=0):
+        return g(fmt, mode, r(a), r(b), FAKE, 4, 512, 256, 256, None, None, None, FAKE, 0, None, 0,
+                 None, None)
+
+    # fprop: A is M_cap x K = 512 x 256, B is G*N x K = 1024 x 256
+    assert call(mxg.Operand(FAKE, FAKE, None, 256, 0, 0), ok) == 1      # A rows
+    assert call(ok, mxg.Operand(FAKE, FAKE, None, 0, 512, 0)) == 1      # B cols
+    assert call(mxg.Operand(FAKE, FAKE, None, 0, 0, 128), ok) == 1      # ld < cols
+    assert call(mxg.Operand(FAKE, FAKE, None, 0, 0, 264), ok) == 2      # 264 bytes
+    # wgrad: A is N x M_cap = 256 x 512
+    assert call(mxg.Operand(FAKE, FAKE, None, 256, 256, 0), ok, mode=1) == 1
+    # NVFP4 (outer scales present): ld counts elements, two per byte
+    opo = mxg.Operand(FAKE, FAKE, FAKE, 0, 0, 0)
+    assert call(mxg.Operand(FAKE, FAKE, FAKE, 0, 0, 257), opo, fmt=2) == 2   # odd
+    assert call(mxg.Operand(FAKE, FAKE, FAKE, 0, 0, 272), opo, fmt=2) == 2   # 136 bytes
+
+
+@no_device_only
 def test_dequantize_argument_errors(lib):
     L = lib
     assert L.mxg_dequantize(1, 1, None, FAKE, None, 128, 128, FAKE, 0, None) == 1
