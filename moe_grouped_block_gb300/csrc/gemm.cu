@@ -249,11 +249,45 @@ __device__ __forceinline__ void build_group_tables(const GemmParams& p, int32_t*
 }
 
 // Four consecutive fp32 values at p (16-byte aligned when vec, else any
-// 4-byte alignment).  Callers pass addresses that are the same for every
-// lane of the warp, so each load is a single broadcast transaction.
+// 4-byte alignment).
 __device__ __forceinline__ float4 load4(const float* p, bool vec) {
   if (vec) return *reinterpret_cast<const float4*>(p);
   return make_float4(p[0], p[1], p[2], p[3]);
+}
+
+// Column operands of an epilogue warp's 128 columns, read once per unit
+// before the accumulator is (in flight while the warp waits for it): lane l
+// holds columns 4l .. 4l+3 of the NVFP4 column outer scales (cs) and of the
+// bias (bs); column j is lane j / 4's component j % 4, fetched with a
+// shuffle.  (Loading them per 16-column chunk instead put a load latency in
+// front of every chunk: the NVFP4 epilogue took twice as long.)
+struct EpiCols {
+  float4 cs, bs;
+};
+
+template <bool NVF4>
+__device__ __forceinline__ EpiCols epi_cols(const GemmParams& p, const TileInfo& ti, uint32_t col0,
+                                            uint32_t lane) {
+  EpiCols e;
+  e.cs = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+  e.bs = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (ti.c_col + col0 >= p.out_cols) return e;  // upper half of a half-wide unit: not stored
+  if (NVF4)  // fprop: per weight row; wgrad: per (group, column) of X
+    e.cs = load4(p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row +
+                     col0 + 4 * lane,
+                 p.vec_col);
+  if (p.bias)
+    e.bs = load4(p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0 + 4 * lane,
+                 p.vec_col);
+  return e;
+}
+
+// Component j % 4 of lane j / 4's value (j a compile-time constant after
+// unrolling; every lane of the warp takes part).
+__device__ __forceinline__ float col_value(const float4& v4, int j) {
+  const int c = j & 3;
+  const float x = c == 0 ? v4.x : (c == 1 ? v4.y : (c == 2 ? v4.z : v4.w));
+  return __shfl_sync(0xFFFFFFFFu, x, j >> 2);
 }
 
 // One output row of the epilogue: 128 accumulator columns (v, four loads of
@@ -264,23 +298,20 @@ __device__ __forceinline__ float4 load4(const float* p, bool vec) {
 // skipped.  Each thread owns a row, so a store instruction touches 32 rows:
 // with a 32-byte-aligned C every store fills whole 32-byte sectors (16 bf16
 // or 8 fp32 per store), else 16-byte stores are used.  The column operands
-// (NVFP4 column outer scales, bias) are the same for all lanes and are read
-// four at a time; beta and bias checks are made once per row, not per element.
+// (NVFP4 column outer scales, bias) come from ec by shuffle, so every lane
+// of the warp runs the transform (rows past row_end only skip the loads and
+// stores); beta and bias checks are made once per row, not per element.
 template <bool NVF4>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
-                                             uint32_t col0, uint32_t (&v)[4][32], bool has_k) {
-  if (row >= ti.row_end || ti.c_col + col0 >= p.out_cols) return;
+                                             uint32_t col0, uint32_t (&v)[4][32], bool has_k,
+                                             const EpiCols& ec) {
+  if (ti.c_col + col0 >= p.out_cols) return;  // warp-uniform
+  const bool valid = row < ti.row_end;
   const int64_t cbase = row * p.out_cols + ti.c_col + col0;
   const float alpha = p.alpha ? p.alpha[ti.g] : 1.0f;
-  const float beta = p.beta ? p.beta[ti.g] : 0.0f;
-  const float* bs =
-      p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0 : nullptr;
-  float rs = 1.0f;
-  const float* cs = nullptr;
-  if (NVF4) {  // fprop: per-row / per-weight-row; wgrad: per (group, column) of dY / X
-    rs = p.a_outer[row];
-    cs = p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row + col0;
-  }
+  const float beta = valid && p.beta ? p.beta[ti.g] : 0.0f;  // old C read for valid rows only
+  const bool bs = p.bias != nullptr;
+  const float rs = NVF4 ? (valid ? p.a_outer[row] : 0.0f) : 1.0f;
   // 16 columns at a time (32 bytes of bf16 or 64 of fp32), transformed in
   // place in the accumulator registers
 #pragma unroll
@@ -288,19 +319,12 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
     uint32_t* a = &v[k >> 1][16 * (k & 1)];
     const int j0 = 16 * k;  // first column of the 16
 #pragma unroll
-    for (int e = 0; e < 16; e += 4) {
-      float4 s4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f), b4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (NVF4) s4 = load4(cs + j0 + e, p.vec_col);
-      if (bs) b4 = load4(bs + j0 + e, p.vec_col);
-      const float sc[4] = {s4.x, s4.y, s4.z, s4.w}, bi[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float x = has_k ? __uint_as_float(a[e + i]) : 0.0f;
-        if (NVF4) x = x * rs * sc[i];
-        x *= alpha;
-        if (bs) x += bi[i];
-        a[e + i] = __float_as_uint(x);
-      }
+    for (int e = 0; e < 16; ++e) {
+      float x = has_k ? __uint_as_float(a[e]) : 0.0f;
+      if (NVF4) x = x * rs * col_value(ec.cs, j0 + e);
+      x *= alpha;
+      if (bs) x += col_value(ec.bs, j0 + e);
+      a[e] = __float_as_uint(x);
     }
     if (p.out_bf16) {
       uint16_t* dst = static_cast<uint16_t*>(p.C) + cbase + j0;
@@ -318,7 +342,8 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
         for (int q = 0; q < 8; ++q)
           w[q] = cvt_bf16x2(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1]));
       }
-      if (p.c_align32) {
+      if (!valid) {
+      } else if (p.c_align32) {
         st_global_32B(dst, w);
       } else {
         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -341,7 +366,8 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
 #pragma unroll
           for (int q = 0; q < 8; ++q) w[q] = a[8 * h + q];
         }
-        if (p.c_align32) {
+        if (!valid) {
+        } else if (p.c_align32) {
           st_global_32B(dst, w);
         } else {
           reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -533,6 +559,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
     uint32_t acc = 0, acc_phase = 0;
     for (int64_t t = unit0; t < total_tiles; t += ustride) {
       const TileInfo ti = map_tile<BN, BK, EPB>(t, p, row_off, tile_off);
+      const EpiCols ec = epi_cols<NVF4>(p, ti, col0, lane);  // in flight during the wait
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -550,7 +577,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, ACC, NVF4, BK>::kThreads, 
         acc = 0;
         acc_phase ^= 1u;
       }
-      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k);
+      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k, ec);
     }
   }
 
@@ -659,15 +686,28 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     const int g = lo;
     const int64_t mu = (((prow_off[g + 1] - prow_off[g]) >> 7) + 1) >> 1;
     const int64_t local = t - tile_off[g];
-    // fprop: column unit, then row unit (the clusters in flight share one
-    // weight tile and the expert's activation rows stay in L2).  dgrad: row
-    // unit, then column unit: its contraction runs over the FFN width, so an
-    // expert's dY rows (up to tens of MB) are read by every column unit; with
-    // the columns innermost a wave reads a few row units' dY once and keeps the
-    // expert's transposed weight slab in L2 for the next wave
-    const int64_t ncu = (p.out_cols + 255) >> 8;
-    const int64_t n_tile = p.mode == 2 ? local % ncu : local / mu;
-    const int64_t mu_i = p.mode == 2 ? local / ncu : local % mu;
+    // fprop: column unit, then row unit: the clusters in flight share one
+    // weight tile and the expert's activation rows stay in L2.  dgrad (whose
+    // contraction runs over the FFN width, so that an expert's dY rows and
+    // its transposed weight slab are tens of MB each): the same order while
+    // the expert's dY rows fit in an L2 budget; else blocks of column units
+    // whose weight tiles fit that budget, walked row unit by row unit, so
+    // that the block's weight tiles stay in L2 and each dY row unit is read
+    // once per block.
+    int64_t n_tile = local / mu, mu_i = local % mu;
+    if (p.mode == 2) {
+      constexpr int64_t kL2Budget = 32ll << 20;
+      const int64_t ncu = (p.out_cols + 255) >> 8;
+      if ((prow_off[g + 1] - prow_off[g]) * p.N > kL2Budget) {
+        int64_t cb = kL2Budget / (256 * p.N);
+        cb = cb < 1 ? 1 : (cb > ncu ? ncu : cb);
+        const int64_t blk = local / (mu * cb);
+        const int64_t width = (blk + 1) * cb <= ncu ? cb : ncu - blk * cb;
+        const int64_t rem = local - blk * mu * cb;
+        mu_i = rem / width;
+        n_tile = blk * cb + rem % width;
+      }
+    }
     ti.g = g;
     ti.a_row = row_off[g] + 256 * mu_i + 128 * rank;
     ti.a_sf_row = prow_off[g] + 256 * mu_i + 128 * rank;
@@ -941,6 +981,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     uint32_t acc_phase = 0;
     for (int64_t t = unit0; t < total_units; t += ustride) {
       const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
+      const EpiCols ec = epi_cols<NVF4>(p, ti, col0, lane);  // in flight during the wait
       if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -958,7 +999,7 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty_even);
       acc_phase ^= 1u;
-      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k);
+      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k, ec);
     }
   }
 
