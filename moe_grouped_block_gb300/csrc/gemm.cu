@@ -113,7 +113,10 @@ struct TileInfo {
   int64_t a_row, b_row;      // first row of the A / B tile (TMA coordinate 1)
   int64_t a_sf_row;          // row of A's scales: the padded row when groups are unaligned
   int64_t kb_count;          // K blocks (BK bytes) of this tile
-  int64_t a_kb0, b_kb0;      // first K block of A and of B
+  int64_t a_kb0, b_kb0;      // single-CTA kernel: first K block of A and of B
+  int64_t a_k0, b_k0;        // CTA-pair kernel: first contraction element of A and of B
+  int last_mmas;             // CTA-pair kernel: MMAs of the last K block (a wgrad group
+                             // may end inside it; the others run all of theirs)
   int64_t c_row, c_col;      // top-left output element
   int64_t row_end;           // rows of C at or beyond this are not written
   bool half_n;               // CTA-pair unit whose last 128 output columns are past the
@@ -713,8 +716,9 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     ti.a_sf_row = prow_off[g] + 256 * mu_i + 128 * rank;
     ti.b_row = (p.mode == 0 ? static_cast<int64_t>(g) * p.N : 0) + 256 * n_tile;
     ti.kb_count = p.kb_uniform;
-    ti.a_kb0 = 0;
-    ti.b_kb0 = p.mode == 0 ? 0 : (static_cast<int64_t>(g) * p.N) / (BK * EPB);
+    ti.a_k0 = 0;
+    ti.b_k0 = p.mode == 0 ? 0 : static_cast<int64_t>(g) * p.N;
+    ti.last_mmas = BK / 32;
     ti.c_row = ti.a_row;
     ti.c_col = 256 * n_tile;
     ti.row_end = row_off[g + 1];
@@ -727,8 +731,13 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     ti.a_row = 256 * nu_i + 128 * rank;
     ti.a_sf_row = ti.a_row;
     ti.b_row = 256 * k_tile;
-    ti.kb_count = (prow_off[g + 1] - prow_off[g]) / (BK * EPB);
-    ti.a_kb0 = ti.b_kb0 = prow_off[g] / (BK * EPB);
+    // the group's padded rows (a multiple of 128) in K blocks of BK * EPB
+    // elements; when they end inside the last block only its first MMAs
+    // (32 bytes, i.e. 32 * EPB elements, each) belong to the group
+    const int64_t rows = prow_off[g + 1] - prow_off[g], kel = BK * EPB;
+    ti.kb_count = (rows + kel - 1) / kel;
+    ti.last_mmas = static_cast<int>((rows - (ti.kb_count - 1) * kel) / (32 * EPB));
+    ti.a_k0 = ti.b_k0 = prow_off[g];
     ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
     ti.c_col = ti.b_row;
     ti.row_end = static_cast<int64_t>(g + 1) * p.N;
@@ -832,22 +841,26 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
           }
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const uint32_t sfb_bar = mapa_shared(sffull_bar(stage), 0);
-          const int64_t ka = ti.a_kb0 + kb, kbb = ti.b_kb0 + kb;
+          // first contraction element of this K block in A and in B (a
+          // multiple of 128: a scale tile boundary)
+          const int64_t ea = ti.a_k0 + kb * (BK * EPB), eb = ti.b_k0 + kb * (BK * EPB);
           // scale tiles first, on their own barrier: this CTA's A band, both B
           // bands of the unit.  They land well before the operand tiles, so
-          // the copy warps move them into tensor memory meanwhile.
-          const int64_t a_atom = ka * Cfg::kAtomsK;
-          const int64_t b_atom = kbb * Cfg::kAtomsK;
+          // the copy warps move them into tensor memory meanwhile.  A scale
+          // tile covers 128 (MXFP8) or 64 (NVFP4) elements of the contraction.
+          const int64_t a_atom = ea / (NVF4 ? 64 : 128);
+          const int64_t b_atom = eb / (NVF4 ? 64 : 128);
           tma_load_2d_pair(ssfa, &tmap_sfa, sfb_bar, 0,
                            static_cast<int32_t>(a_band * p.a_atoms_row + a_atom));
           tma_load_3d_pair(ssfb, &tmap_sfb, sfb_bar, 0, static_cast<int32_t>(b_atom), b_band);
 #pragma unroll
           for (int sub = 0; sub < Cfg::kSubTiles; ++sub) {
             const uint32_t off = static_cast<uint32_t>(sub * 128 * Cfg::kSubK);
-            tma_load_2d_pair(sa + off, &tmap_a, fb, static_cast<int32_t>(ka * BK + sub * Cfg::kSubK),
+            tma_load_2d_pair(sa + off, &tmap_a, fb,
+                             static_cast<int32_t>(ea / EPB + sub * Cfg::kSubK),
                              static_cast<int32_t>(ti.a_row));
             tma_load_2d_pair(sb + off, &tmap_b, fb,
-                             static_cast<int32_t>(kbb * BK + sub * Cfg::kSubK), b_half);
+                             static_cast<int32_t>(eb / EPB + sub * Cfg::kSubK), b_half);
           }
           issued_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -888,8 +901,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
           const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
           const uint32_t idesc = ti.half_n ? Cfg::kIdescN128 : Cfg::kIdesc;
+          const int nmma = kb + 1 == ti.kb_count ? ti.last_mmas : Cfg::kMmas;
 #pragma unroll
           for (int kk = 0; kk < Cfg::kMmas; ++kk) {
+            if (kk >= nmma) break;  // rows of the next group (wgrad): loaded, not used
             // K step kk: sub-tile kk / kMmasPerSub, 32 bytes further along the
             // row per step within it (16-byte units)
             const int sub = kk / Cfg::kMmasPerSub, ks = kk % Cfg::kMmasPerSub;
@@ -1139,14 +1154,19 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
   p.b_atoms_row = b_kdim / blk / 4;
   const bool pair_kernel = tile_n == 0 && b_rows >= 256;
   if (unaligned && !(pair_kernel && !nvfp4)) return cudaErrorInvalidValue;
-  // bytes of K per pipeline stage.  NVFP4 wgrad needs 64 (a 128-row group is
-  // 64 bytes of E2M1 along the contraction), and so does an NVFP4 fprop whose
-  // K is not a multiple of 256 elements.  256-byte stages: MXFP8 fprop on the
-  // CTA-pair kernel with K % 256 == 0 (measured: fine-grained fprop 2.5 %
-  // faster, Mixtral fprop unchanged; dgrad lost 2 % with 3 stages instead of
-  // 6 and keeps 128, as does wgrad, whose 128-row groups need it).
-  const bool need64 = nvfp4 && (mode == 1 || (K % 256) != 0);
-  const bool wide = !nvfp4 && stage_bytes == 0 && pair_kernel && mode == 0 && K % 256 == 0;
+  // bytes of K per pipeline stage.  An NVFP4 fprop whose K is not a multiple
+  // of 256 elements needs 64, and so does NVFP4 wgrad on the single-CTA
+  // kernel (a 128-row group is 64 bytes of E2M1 along the contraction).
+  // 256-byte stages: MXFP8 fprop on the CTA-pair kernel with K % 256 == 0
+  // (measured: fine-grained fprop 2.5 % faster, Mixtral fprop unchanged;
+  // dgrad lost 2 % with 3 stages instead of 6 and keeps 128) and MXFP8 wgrad
+  // on it.  The CTA-pair kernel lets a wgrad group end inside its last K
+  // block (only that block's first MMAs run), so wgrad takes the wide stages
+  // there: 8 MMAs per stage (MXFP8), 4 (NVFP4, 128 bytes), where 4 and 2
+  // left the MMA thread's per-stage wait and commit on the critical path.
+  const bool need64 = nvfp4 && ((mode == 1 && !pair_kernel) || (mode == 0 && (K % 256) != 0));
+  const bool wide = !nvfp4 && stage_bytes == 0 && pair_kernel &&
+                    ((mode == 0 && K % 256 == 0) || mode == 1);
   const int BKB = need64 ? 64 : (wide ? 256 : 128);
   p.kb_uniform = mode == 0 ? (nvfp4 ? K / 2 : K) / BKB : (mode == 2 ? N / BKB : 0);
   p.out_cols = mode == 0 ? N : K;
