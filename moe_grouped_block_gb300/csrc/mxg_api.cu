@@ -226,7 +226,7 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
                                                      cols, group_ws, G,
                                                      static_cast<uint8_t*>(q_col), sf_col,
                                                      outer_col, sms, s),
-                  4);
+                  1);
 }
 
 static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,

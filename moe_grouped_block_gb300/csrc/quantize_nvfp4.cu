@@ -321,8 +321,19 @@ __global__ void __launch_bounds__(64 * kNvRowPairs, 2)
 // the group's rows; R2 then runs down the column in 16-row blocks.  Output
 // qT[k, m/2] (rows m, m+1 in the low / high nibble), E4M3 scales swizzled
 // over [cols, cap/16], outer [G, cols].
-// Four launches: zero the outer buffer; per-tile column amax folded in with
-// atomicMax (order-independent, so deterministic); quantize; outer = A/2688.
+//
+// One launch.  A work unit is one group's rows in a strip of 64 columns, and
+// one CTA owns it whole: pass 1 streams the strip's 256-row tiles (32 KB; TMA,
+// a ring of three buffers, two loads ahead) for the column amax and writes
+// the outer scales; pass 2 streams the same tiles again, in reverse order,
+// and quantizes, finding most of them still in L2.  So the input crosses
+// HBM about once and a half instead of twice, and no atomics, no zeroing or
+// finishing launch and no wait on another CTA are needed.  Units are dealt
+// to the CTAs in rounds, forwards and backwards in turn, over the groups
+// sorted by size (up to 64 groups; unsorted beyond), so that every CTA gets
+// about the same number of rows.  (Measured against it and slower: 32- and
+// size-dependent strip widths, deeper buffer rings with one CTA per SM, and
+// three CTAs per SM with two buffers.)
 // ------------------------------------------------------------------------
 
 // Sanitised row offsets of the groups into shared memory (warp 0).
@@ -357,172 +368,242 @@ __device__ __forceinline__ void build_row_offsets(const int64_t* ws, int G, int6
   if (lane == 0) row_off[G] = min(carry, cap);
 }
 
-__device__ __forceinline__ int group_of_row(const int64_t* row_off, int G, int64_t m) {
-  int lo = 0, hi = G;  // largest g with row_off[g] <= m
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (row_off[mid] <= m)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  return lo;
-}
+constexpr int kNvsCols = 64;                       // columns of a strip (128-byte rows)
+constexpr int kNvsRows = 256;                      // rows of a tile (one TMA box)
+constexpr int kNvsPairs = kNvsCols / 2;            // column pairs: the lanes of a warp
+constexpr int kNvsTileBytes = kNvsRows * kNvsCols * 2;
+constexpr int kNvsBufs = 3;                        // tile buffers: loads run 2 tiles ahead
+constexpr int kNvsSortMax = 64;                    // groups sorted by size up to this many
+// dynamic shared memory: the tile ring, alignment slack; then the row offsets
+// (G + 1 int64) and the unit order (G int32)
+constexpr int kNvsSmem = kNvsBufs * kNvsTileBytes + 1024;
 
-__global__ void nvfp4_col_zero_kernel(float* __restrict__ outer, int64_t n) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    outer[i] = 0.0f;
-}
+// A unit of the colwise quantize: group g's rows [r0, r0 + rows) in the
+// 64-column strip at k0, and its tiles.
+struct StripUnit {
+  int64_t r0, rows, k0;
+  int g, nt;
+};
 
-// The two passes over 128 x 128 bf16 tiles, staged in shared memory by TMA
-// (double buffered: thread 0 loads the CTA's next tile while all threads work
-// on the current one).  Thread (column pair cp, 32-row quarter j); a 32-bit
-// word of the tile holds columns 2cp and 2cp+1 of one row.  A tile lies in
-// one group (groups are multiples of 128 rows).
-//   AMAX:  column amax over the tile (packed bf16 maximum, both columns at
-//          once), reduced over the four quarters in shared memory, folded into
-//          outer[g, k] with atomicMax on the float bits (non-negative floats
-//          order as integers, so the result does not depend on the order).
-//   QUANT: the 16-row blocks of each column with the group's column amax,
-//          written transposed (16 bytes per column and quarter), scales staged
-//          and stored as two 512-byte swizzle tiles.
-constexpr int kNvColTileBytes = 128 * 128 * 2;
-// dynamic shared memory: two tiles, alignment slack, then the G + 1 row offsets
-constexpr int kNvColSmem = 2 * kNvColTileBytes + 1024;
-
-template <bool QUANT>
-__global__ void __launch_bounds__(256, 3)
-    nvfp4_col_tiles_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
+__global__ void __launch_bounds__(256)
+    nvfp4_col_strip_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                            const int64_t* __restrict__ ws, int G, float* __restrict__ outer,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT) {
-  extern __shared__ uint8_t csm_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(csm_raw) + 1023) &
+  extern __shared__ uint8_t nsm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(nsm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bars[2];
+  __shared__ uint64_t bars[kNvsBufs];
   __shared__ int abort_s;
-  __shared__ float part[4][128];
-  __shared__ __align__(16) uint8_t sf_s[2][512];
-  int64_t* row_off = reinterpret_cast<int64_t*>(sm + 2 * kNvColTileBytes);
+  __shared__ uint32_t red[256];  // pass 1: per (slice, column pair), packed |x| max
+  __shared__ float Ss[kNvsCols], As[kNvsCols];
+  __shared__ float sixth[128];  // sixth[M - 128] = RN(M / 6) for the 8-bit significands M
   const int Gt = ws ? G : 1;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
+  int64_t* row_off = reinterpret_cast<int64_t*>(sm + kNvsBufs * kNvsTileBytes);
+  int32_t* order = reinterpret_cast<int32_t*>(row_off + Gt + 1);
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  if (tid == 0) {
+    for (int i = 0; i < kNvsBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
     abort_s = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x < 32) build_row_offsets(ws, G, cap, row_off);
+  if (warp == 0) build_row_offsets(ws, G, cap, row_off);
+  if (tid < 128) sixth[tid] = __fdiv_rn(static_cast<float>(128 + tid), 6.0f);
+  __syncthreads();
+  if (warp == 0) {  // units go largest group first (ties: group index)
+    for (int g = static_cast<int>(lane); g < Gt; g += 32) {
+      int rank = g;
+      if (Gt <= kNvsSortMax) {
+        const int64_t sg = row_off[g + 1] - row_off[g];
+        rank = 0;
+        for (int h = 0; h < Gt; ++h) {
+          const int64_t sh = row_off[h + 1] - row_off[h];
+          rank += (sh > sg || (sh == sg && h < g)) ? 1 : 0;
+        }
+      }
+      order[rank] = g;
+    }
+  }
   __syncthreads();
   volatile int* abort_flag = &abort_s;
-  const int64_t kt = cols >> 7, tiles = (row_off[Gt] >> 7) * kt;
-  // the QUANT pass walks the tiles in the reverse order of the AMAX pass, so
-  // that it starts on the tiles the AMAX pass read last, still held in L2
-  auto tile_of = [&](int64_t t) { return QUANT ? tiles - 1 - t : t; };
-  auto issue = [&](int64_t t, int b) {
-    const uint32_t bar = smem_u32(&bars[b]);
-    const int64_t tt = tile_of(t);
-    mbar_arrive_expect_tx(bar, kNvColTileBytes);
-    tma_load_2d(smem_u32(sm + b * kNvColTileBytes), &tmap_x, bar,
-                static_cast<int32_t>((tt % kt) << 7), static_cast<int32_t>((tt / kt) << 7));
+  const uint32_t S = static_cast<uint32_t>(cols / kNvsCols);
+  const uint32_t units = static_cast<uint32_t>(Gt) * S;
+  const uint32_t P = gridDim.x, c = blockIdx.x;
+  // the CTA's n-th unit: rounds of P units dealt forwards in even rounds and
+  // backwards in odd ones; false past the last
+  auto unit_of = [&](uint32_t n, StripUnit& u) -> bool {
+    const uint32_t i = n * P + ((n & 1u) ? P - 1 - c : c);
+    if (i >= units) return false;
+    u.g = order[i / S];
+    u.k0 = static_cast<int64_t>(i % S) * kNvsCols;
+    u.r0 = row_off[u.g];
+    u.rows = row_off[u.g + 1] - u.r0;
+    u.nt = static_cast<int>((u.rows + kNvsRows - 1) / kNvsRows);
+    return true;
   };
-  if (threadIdx.x == 0 && static_cast<int64_t>(blockIdx.x) < tiles) {
-    prefetch_tmap(&tmap_x);
-    issue(blockIdx.x, 0);
+
+  // Thread 0's load cursor runs kNvsBufs - 1 tiles ahead of the work: unit
+  // an (decoded in au), tile ordinal aj within it (pass 1: tiles 0..nt-1,
+  // then pass 2: tiles nt-1..0).
+  uint32_t an = 0;
+  int aj = 0;
+  StripUnit au;
+  bool ahead = false;
+  auto ahead_first = [&]() {  // the first unit with rows at or after an
+    for (;; ++an) {
+      if (!unit_of(an, au)) return false;
+      if (au.rows > 0) return true;
+    }
+  };
+  auto issue = [&](int b) {
+    const int64_t j = aj < au.nt ? aj : 2 * au.nt - 1 - aj;
+    const uint32_t bar = smem_u32(&bars[b]);
+    mbar_arrive_expect_tx(bar, kNvsTileBytes);
+    tma_load_2d(smem_u32(sm + b * kNvsTileBytes), &tmap_x, bar, static_cast<int32_t>(au.k0),
+                static_cast<int32_t>(au.r0 + j * kNvsRows));
+    if (++aj == 2 * au.nt) {
+      aj = 0;
+      ++an;
+      ahead = ahead_first();
+    }
+  };
+  uint32_t parity = 0u, pending = 0u;
+  if (tid == 0) {
+    ahead = ahead_first();
+    if (ahead) prefetch_tmap(&tmap_x);
+    for (int i = 0; i < kNvsBufs - 1 && ahead; ++i) {
+      issue(i);
+      pending |= 1u << i;
+    }
   }
-  const uint32_t cp = threadIdx.x & 63u, j = threadIdx.x >> 6;
-  uint32_t parity = 0u, pending = static_cast<int64_t>(blockIdx.x) < tiles ? 1u : 0u;
+
   int b = 0;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, b ^= 1) {
-    if (threadIdx.x == 0 && t + gridDim.x < tiles) {
-      issue(t + gridDim.x, b ^ 1);
-      pending |= 1u << (b ^ 1);
+  const int64_t C4 = cap >> 6;  // swizzle tiles per 128-column band along the rows
+  // thread: column pair cp (columns 2 cp, 2 cp + 1 of the strip), rows
+  // 32 slice .. 32 slice + 31 of every tile
+  const uint32_t cp = tid % kNvsPairs, slice = tid / kNvsPairs;
+  StripUnit u;
+  for (uint32_t n = 0; unit_of(n, u); ++n) {
+    if (u.rows == 0) {  // a group without rows: its outer scales are 0
+      if (tid < kNvsCols) outer[static_cast<int64_t>(u.g) * cols + u.k0 + tid] = 0.0f;
+      continue;
     }
-    if (!mbar_wait(smem_u32(&bars[b]), (parity >> b) & 1u, abort_flag, nullptr)) *abort_flag = 1;
-    parity ^= 1u << b;
-    pending &= ~(1u << b);
-    __syncthreads();
-    if (*abort_flag) break;
-    const int64_t tt = tile_of(t), m0 = (tt / kt) << 7, k0 = (tt % kt) << 7;
-    const int g = group_of_row(row_off, Gt, m0);
-    const uint32_t* col = reinterpret_cast<const uint32_t*>(sm + b * kNvColTileBytes) +
-                          (32 * j) * 64 + cp;
-    if (!QUANT) {
-      uint32_t m = 0;
+    uint32_t colmax = 0;  // pass 1 running packed maximum
+    for (int job = 0; job < 2 * u.nt; ++job) {
+      if (!mbar_wait(smem_u32(&bars[b]), (parity >> b) & 1u, abort_flag, nullptr)) *abort_flag = 1;
+      parity ^= 1u << b;
+      pending &= ~(1u << b);
+      __syncthreads();  // the previous job's buffer is free; Ss / As of this unit are set (pass 2)
+      if (*abort_flag) break;
+      if (tid == 0 && ahead) {
+        const int bl = (b + kNvsBufs - 1) % kNvsBufs;  // the previous job's buffer
+        issue(bl);
+        pending |= 1u << bl;
+      }
+      const bool pass1 = job < u.nt;
+      const int64_t j = pass1 ? job : 2 * u.nt - 1 - job;
+      const int64_t valid = min(static_cast<int64_t>(kNvsRows), u.rows - j * kNvsRows);
+      const uint32_t* tile = reinterpret_cast<const uint32_t*>(sm + b * kNvsTileBytes);
+      if (pass1) {
+        // column maximum of |x| over this thread's 32 rows, both columns of
+        // the pair at once (packed bf16, exact)
+        if (static_cast<int64_t>(32 * slice) < valid) {
 #pragma unroll 8
-      for (int i = 0; i < 32; ++i) m = bf16x2_max_abs(m, col[i * 64]);
-      part[j][2 * cp] = __uint_as_float((m & 0x7FFFu) << 16);
-      part[j][2 * cp + 1] = __uint_as_float(m & 0x7FFF0000u);
-      __syncthreads();
-      if (threadIdx.x < 128) {
-        const uint32_t c = threadIdx.x;
-        const float a = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
-        atomicMax(reinterpret_cast<unsigned int*>(outer + static_cast<int64_t>(g) * cols + k0 + c),
-                  __float_as_uint(a));
-      }
-    } else {
-      uint32_t w[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = col[i * 64];
-      // 16-row block amax of both columns at once (packed bf16 maximum)
-      uint32_t bm[2];
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = bf16x2_max_abs(m, w[16 * blk + i]);
-        bm[blk] = m;
-      }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t kk = 2 * cp + c;
-        const float A = outer[static_cast<int64_t>(g) * cols + k0 + kk];
-        const bool zero = !(A > 0.f);
-        const float S = zero ? 0.f : __fdiv_rn(2688.0f, A);
-        uint32_t o[4];
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          const float ab = c ? __uint_as_float(bm[blk] & 0x7FFF0000u)
-                             : __uint_as_float((bm[blk] & 0x7FFFu) << 16);
-          uint32_t sbyte = 0;
-          if (!zero) sbyte = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ab, 6.0f), S), 0.f) & 0x7Fu;
-          const float sbv = ue4m3_value(sbyte);
-          const float ratio = sbv == 0.f ? 0.f : __fdiv_rn(S, sbv);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {  // byte i: rows 2i (low nibble), 2i+1 of this 8-row run
-              const int r = 16 * blk + 8 * h + 2 * i;
-              const float v0 = c ? bf16hi(w[r]) : bf16lo(w[r]);
-              const float v1 = c ? bf16hi(w[r + 1]) : bf16lo(w[r + 1]);
-              uint32_t byte;
-              if (sbv == 0.f) {
-                byte = (signbit(v0) ? 0x8u : 0u) | (signbit(v1) ? 0x80u : 0u);
-              } else {
-                byte = cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio));
-              }
-              word |= byte << (8 * i);
-            }
-            o[2 * blk + h] = word;
-          }
-          const uint32_t sc = 2 * j + blk;  // scale column within the tile (0..7)
-          sf_s[sc >> 2][(kk & 31u) * 16 + (kk >> 5) * 4 + (sc & 3u)] = static_cast<uint8_t>(sbyte);
+          for (int i = 0; i < 32; ++i)
+            colmax = bf16x2_max_abs(colmax, tile[(32 * slice + i) * kNvsPairs + cp]);
         }
-        *reinterpret_cast<uint4*>(qT + (k0 + kk) * (cap >> 1) + ((m0 + 32 * j) >> 1)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+        if (job + 1 == u.nt) {
+          red[tid] = colmax & 0x7FFF7FFFu;  // = red[slice * kNvsPairs + cp]
+          __syncthreads();
+          if (tid < kNvsCols) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int q = 0; q < 256 / kNvsPairs; ++q) m = bf16x2_max_abs(m, red[q * kNvsPairs + (tid >> 1)]);
+            const float A = (tid & 1) ? bf16hi(m & 0x7FFF7FFFu) : bf16lo(m & 0x7FFF7FFFu);
+            As[tid] = A;
+            Ss[tid] = A > 0.f ? __fdiv_rn(2688.0f, A) : 0.f;
+            outer[static_cast<int64_t>(u.g) * cols + u.k0 + tid] =
+                A > 0.f ? __fdiv_rn(A, 2688.0f) : 0.0f;
+          }
+          // Ss / As are read in pass 2, after the next job's barrier
+        }
+      } else if (static_cast<int64_t>(32 * slice) < valid) {
+        // columns 2 cp, 2 cp + 1 (one 32-bit word), rows 32 slice .. 32 slice
+        // + 31 of the tile: two 16-row blocks of each column
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = tile[(32 * slice + i) * kNvsPairs + cp];
+        uint32_t bm[2];  // block maxima of |x|, both columns packed (exact)
+#pragma unroll
+        for (int bk = 0; bk < 2; ++bk) {
+          uint32_t mm = 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mm = bf16x2_max_abs(mm, w[16 * bk + i]);
+          bm[bk] = mm & 0x7FFF7FFFu;
+        }
+        const int64_t m = u.r0 + j * kNvsRows + 32 * slice;  // first row
+        const int64_t cb = m >> 4;                     // first 16-row block (even)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t kc = 2 * cp + cc;
+          const float A = As[kc], Sv = Ss[kc];
+          const bool zero = !(A > 0.f);
+          uint32_t o[4];
+          uint32_t sword = 0;
+#pragma unroll
+          for (int bk = 0; bk < 2; ++bk) {
+            const float ab = cc ? bf16hi(bm[bk]) : bf16lo(bm[bk]);
+            uint32_t sbyte = 0;
+            if (!zero) {
+              // RN(ab / 6): ab is a bf16 value, M * 2^E with an 8-bit significand
+              // M; for ab >= 2^-123 the quotient is a normal fp32 and equals
+              // RN(M / 6) * 2^E exactly (a power-of-two scaling commutes with
+              // rounding), so the table entry is scaled instead of dividing
+              const uint32_t ub = __float_as_uint(ab);
+              const uint32_t ex = ub >> 23;  // biased exponent (ab >= 0)
+              const float q6 = ex >= 4u ? __uint_as_float(__float_as_uint(sixth[(ub >> 16) & 127u]) +
+                                                          ((ex - 134u) << 23))
+                                        : __fdiv_rn(ab, 6.0f);
+              sbyte = cvt_e4m3x2(__fmul_rn(q6, Sv), 0.f) & 0x7Fu;
+            }
+            const float sbv = ue4m3_value(sbyte);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) o[2 * bk + h] = 0;
+            if (sbv == 0.f) {  // codes are the signs of x
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t w0 = w[16 * bk + 8 * h + 2 * i], w1 = w[16 * bk + 8 * h + 2 * i + 1];
+                  const uint32_t s0 = cc ? (w0 >> 31) : ((w0 >> 15) & 1u);
+                  const uint32_t s1 = cc ? (w1 >> 31) : ((w1 >> 15) & 1u);
+                  o[2 * bk + h] |= ((s0 << 3) | (s1 << 7)) << (8 * i);
+                }
+            } else {
+              const float ratio = __fdiv_rn(Sv, sbv);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t w0 = w[16 * bk + 8 * h + 2 * i], w1 = w[16 * bk + 8 * h + 2 * i + 1];
+                  const float v0 = cc ? bf16hi(w0) : bf16lo(w0), v1 = cc ? bf16hi(w1) : bf16lo(w1);
+                  o[2 * bk + h] |= cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio)) << (8 * i);
+                }
+            }
+            sword |= sbyte << (8 * bk);
+          }
+          const int64_t k = u.k0 + kc;
+          *reinterpret_cast<uint4*>(qT + k * (cap >> 1) + (m >> 1)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint16_t*>(sfT + ((k >> 7) * C4 + (cb >> 2)) * 512 + (k & 31) * 16 +
+                                       ((k & 127) >> 5) * 4 + (cb & 3)) = static_cast<uint16_t>(sword);
+        }
       }
-      __syncthreads();
-      if (threadIdx.x < 64) {
-        const uint32_t a = threadIdx.x >> 5, l = threadIdx.x & 31u;
-        const int64_t atom = (k0 >> 7) * (cap >> 6) + (m0 >> 6) + a;
-        reinterpret_cast<uint4*>(sfT + atom * 512)[l] = reinterpret_cast<const uint4*>(sf_s[a])[l];
-      }
+      b = (b + 1) % kNvsBufs;
     }
-    __syncthreads();  // tile buffer, part[] and the scale staging are reused
+    if (*abort_flag) break;
   }
-  // a prefetch still in flight (only after an abort) lands before the CTA exits
-  if (threadIdx.x == 0)
-    for (int bb = 0; bb < 2; ++bb)
+  // a load still in flight (only after an abort) lands before the CTA exits
+  if (tid == 0)
+    for (int bb = 0; bb < kNvsBufs; ++bb)
       if (pending & (1u << bb)) {
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(smem_u32(&bars[bb]), (parity >> bb) & 1u))
@@ -530,51 +611,28 @@ __global__ void __launch_bounds__(256, 3)
       }
 }
 
-__global__ void nvfp4_col_finalize_kernel(float* __restrict__ outer, int64_t n) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float A = outer[i];
-    outer[i] = A > 0.f ? __fdiv_rn(A, 2688.0f) : 0.0f;
-  }
-}
-
 cudaError_t launch_nvfp4_quantize_colwise(const uint16_t* x, int64_t cap, int64_t cols,
                                           const int64_t* group_ws, int G, uint8_t* qT,
                                           uint8_t* sfT, float* outer, int num_sms,
                                           cudaStream_t stream) {
   const int Gt = group_ws ? G : 1;
-  const int64_t n_outer = static_cast<int64_t>(Gt) * cols;
-  const int gz = static_cast<int>(std::min<int64_t>((n_outer + 255) / 256, num_sms * 4));
-  nvfp4_col_zero_kernel<<<gz, 256, 0, stream>>>(outer, n_outer);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || cap == 0) return e;
-  const int64_t max_tiles = (cap >> 7) * (cols >> 7);
   CUtensorMap tm;
   if (!make_tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, static_cast<uint64_t>(cols),
-                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, 128, 128,
+                    static_cast<uint64_t>(cap), static_cast<uint64_t>(cols) * 2, kNvsCols, kNvsRows,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  auto ka = nvfp4_col_tiles_kernel<false>;
-  auto kq = nvfp4_col_tiles_kernel<true>;
-  const int smem = kNvColSmem + 8 * (Gt + 1);
-  if ((e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
-          cudaSuccess)
-    return e;
-  // persistent grids: as many CTAs as are resident at once
-  auto grid_of = [&](auto kern) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    return static_cast<int>(std::min<int64_t>(max_tiles, static_cast<int64_t>(num_sms) * per_sm));
-  };
-  ka<<<grid_of(ka), 256, smem, stream>>>(tm, cap, cols, group_ws, G, outer, qT, sfT);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kq<<<grid_of(kq), 256, smem, stream>>>(tm, cap, cols, group_ws, G, outer, qT, sfT);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  nvfp4_col_finalize_kernel<<<gz, 256, 0, stream>>>(outer, n_outer);
+  auto kern = nvfp4_col_strip_kernel;
+  const int smem = kNvsSmem + 8 * (Gt + 1) + 4 * Gt;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // persistent grid: as many CTAs as are resident at once, at most one per unit
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t units = static_cast<int64_t>(Gt) * (cols / kNvsCols);
+  const int grid = static_cast<int>(std::min<int64_t>(units, static_cast<int64_t>(num_sms) * per_sm));
+  kern<<<grid, 256, smem, stream>>>(tm, cap, cols, group_ws, G, outer, qT, sfT);
   return cudaGetLastError();
 }
 
