@@ -645,9 +645,9 @@ struct PairCfg {
   static constexpr int kTmemCols = 512;
   static_assert(BN + STAGES * kSfCols <= kTmemCols, "tensor memory budget");
   static constexpr int kSfCopies = 3 * kAtomsK;  // scale tiles per stage (A, then B bands)
-  // full[S], empty[S], sffull[S], tfull, tempty, drain, sfdrain;
-  // TMEM base; abort flag
-  static constexpr int kBarBytes = 8 * (3 * STAGES + 4) + 16;
+  // full[S], empty[S], sffull[S], tfull, tempty, drain, sfdrain,
+  // info_full[2], info_empty[2], two unit words; TMEM base; abort flag
+  static constexpr int kBarBytes = 8 * (3 * STAGES + 10) + 16;
   static size_t smem_bytes(int G) {
     return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16;
   }
@@ -672,6 +672,16 @@ struct PairCfg {
 // on the padded offsets, so unaligned groups (a last 128-row tile partly past
 // the group) need nothing else: A's data rows start at the group's row
 // offset, its scale rows (a_sf_row) and its colwise slabs at the padded one.
+// a / b for a >= 0, b > 0: the 32-bit division when both fit (always, for
+// the unit counts of any output that fits in memory), the 64-bit one
+// otherwise.  A 64-bit division is a long dependent chain, and the unit
+// decode runs on single threads between units.
+__device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
+  if (((static_cast<uint64_t>(a) | static_cast<uint64_t>(b)) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
 template <int EPB, int BK>
 __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p,
                                                   const int32_t* row_off, const int32_t* prow_off,
@@ -697,18 +707,18 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     // whose weight tiles fit that budget, walked row unit by row unit, so
     // that the block's weight tiles stay in L2 and each dY row unit is read
     // once per block.
-    int64_t n_tile = local / mu, mu_i = local % mu;
+    int64_t n_tile = udiv(local, mu), mu_i = local - n_tile * mu;
     if (p.mode == 2) {
       constexpr int64_t kL2Budget = 32ll << 20;
       const int64_t ncu = (p.out_cols + 255) >> 8;
       if ((prow_off[g + 1] - prow_off[g]) * p.N > kL2Budget) {
-        int64_t cb = kL2Budget / (256 * p.N);
-        cb = cb < 1 ? 1 : (cb > ncu ? ncu : cb);
-        const int64_t blk = local / (mu * cb);
+        int64_t cb = 256 * p.N > kL2Budget ? 1 : udiv(kL2Budget, 256 * p.N);
+        cb = cb > ncu ? ncu : cb;
+        const int64_t blk = udiv(local, mu * cb);
         const int64_t width = (blk + 1) * cb <= ncu ? cb : ncu - blk * cb;
         const int64_t rem = local - blk * mu * cb;
-        mu_i = rem / width;
-        n_tile = blk * cb + rem % width;
+        mu_i = udiv(rem, width);
+        n_tile = blk * cb + (rem - mu_i * width);
       }
     }
     ti.g = g;
@@ -723,10 +733,11 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     ti.c_col = 256 * n_tile;
     ti.row_end = row_off[g + 1];
   } else {
-    const int64_t nu = ((p.N >> 7) + 1) >> 1, kt = (p.K + 255) / 256, tpg = nu * kt;
-    const int g = static_cast<int>(t / tpg);
-    const int64_t local = t % tpg;
-    const int64_t nu_i = local / kt, k_tile = local % kt;
+    const int64_t nu = ((p.N >> 7) + 1) >> 1, kt = (p.K + 255) >> 8, tpg = nu * kt;
+    const int64_t gq = udiv(t, tpg);
+    const int g = static_cast<int>(gq);
+    const int64_t local = t - gq * tpg;
+    const int64_t nu_i = udiv(local, kt), k_tile = local - nu_i * kt;
     ti.g = g;
     ti.a_row = 256 * nu_i + 128 * rank;
     ti.a_sf_row = ti.a_row;
@@ -735,7 +746,7 @@ __device__ __forceinline__ TileInfo map_unit_pair(int64_t t, const GemmParams& p
     // elements; when they end inside the last block only its first MMAs
     // (32 bytes, i.e. 32 * EPB elements, each) belong to the group
     const int64_t rows = prow_off[g + 1] - prow_off[g], kel = BK * EPB;
-    ti.kb_count = (rows + kel - 1) / kel;
+    ti.kb_count = (rows + kel - 1) / kel;  // kel and 32 * EPB: powers of two
     ti.last_mmas = static_cast<int>((rows - (ti.kb_count - 1) * kel) / (32 * EPB));
     ti.a_k0 = ti.b_k0 = prow_off[g];
     ti.c_row = static_cast<int64_t>(g) * p.N + ti.a_row;
@@ -759,7 +770,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* bar_area = smem + STAGES * Cfg::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bar_area);
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * STAGES + 4));
+  // after the stage and accumulator barriers: info_full[2], info_empty[2],
+  // the two published unit words, then the TMEM base and the abort flag
+  uint64_t* info_word = bars + 3 * STAGES + 8;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * STAGES + 10));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_s + 1);
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
@@ -775,6 +789,9 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
   const uint32_t tempty_bar = smem_u32(&bars[3 * STAGES + 1]);
   const uint32_t drain_bar = smem_u32(&bars[3 * STAGES + 2]);
   const uint32_t sfdrain_bar = smem_u32(&bars[3 * STAGES + 3]);
+  auto info_full_bar = [&](uint32_t i) { return smem_u32(&bars[3 * STAGES + 4 + i]); };
+  auto info_empty_bar = [&](uint32_t i) { return smem_u32(&bars[3 * STAGES + 6 + i]); };
+  constexpr uint64_t kInfoKbMask = (1ull << 48) - 1;
   constexpr uint32_t kFirstSfWarp = 2 + Cfg::kEpiWarps;
 
   // ------------------------------------------------------------ set-up
@@ -790,6 +807,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     mbar_init(tempty_bar, 2 * Cfg::kEpiWarps);  // even CTA: both CTAs' epilogue warps
     mbar_init(drain_bar, 1);
     mbar_init(sfdrain_bar, Cfg::kSfWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(info_full_bar(i), 1);                   // the producer
+      mbar_init(info_empty_bar(i), 1 + Cfg::kSfWarps);  // the MMA thread, the scale-copy warps
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -819,8 +840,18 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, last_parity = 0;
       bool ok = true;
-      for (int64_t t = unit0; ok && t < total_units; t += ustride) {
+      for (int64_t t = unit0, u = 0; ok && t < total_units; t += ustride, ++u) {
         const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
+        if (rank == 0) {
+          // publish the unit's shape to the MMA thread and the scale-copy
+          // warps (two slots: at most two units ahead of them)
+          const uint32_t slot = static_cast<uint32_t>(u & 1), ipar = static_cast<uint32_t>((u >> 1) & 1);
+          if (!mbar_wait(info_empty_bar(slot), ipar ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+          info_word[slot] = (static_cast<uint64_t>(ti.kb_count) & kInfoKbMask) |
+                            (static_cast<uint64_t>(ti.last_mmas & 0xFF) << 48) |
+                            (static_cast<uint64_t>(ti.half_n ? 1 : 0) << 56);
+          mbar_arrive(info_full_bar(slot));
+        }
         // this CTA's half of B: rows 128r.. of the unit, or 64r.. when the
         // unit is half wide and its MMAs run with N = 128
         const int32_t b_half = static_cast<int32_t>(ti.b_row + (ti.half_n ? 64 : 128) * rank);
@@ -885,11 +916,18 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     if (lane == 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int64_t t = unit0; ok && t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, 0);
+      for (int64_t t = unit0, u = 0; ok && t < total_units; t += ustride, ++u) {
+        // the unit's shape, as the producer published it
+        const uint32_t slot = static_cast<uint32_t>(u & 1), ipar = static_cast<uint32_t>((u >> 1) & 1);
+        if (!mbar_wait(info_full_bar(slot), ipar, abort_flag, p.status, p.timeout_ns)) break;
+        const uint64_t info = info_word[slot];
+        mbar_arrive(info_empty_bar(slot));
+        const int64_t kb_count = static_cast<int64_t>(info & kInfoKbMask);
+        const int last_mmas = static_cast<int>((info >> 48) & 0xFFu);
+        const bool half_n = (info >> 56) & 1u;
         if (!mbar_wait(tempty_bar, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
         tc_fence_after();
-        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+        for (int64_t kb = 0; kb < kb_count; ++kb) {
           // operands landed, and their scale tiles are in tensor memory
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
@@ -900,8 +938,8 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
           const uint32_t sb = sa + Cfg::kATile;
           const uint32_t sfa_t = tmem_base + Cfg::BN + stage * Cfg::kSfCols;
           const uint32_t sfb_t = sfa_t + Cfg::kSfaCols;
-          const uint32_t idesc = ti.half_n ? Cfg::kIdescN128 : Cfg::kIdesc;
-          const int nmma = kb + 1 == ti.kb_count ? ti.last_mmas : Cfg::kMmas;
+          const uint32_t idesc = half_n ? Cfg::kIdescN128 : Cfg::kIdesc;
+          const int nmma = kb + 1 == kb_count ? last_mmas : Cfg::kMmas;
 #pragma unroll
           for (int kk = 0; kk < Cfg::kMmas; ++kk) {
             if (kk >= nmma) break;  // rows of the next group (wgrad): loaded, not used
@@ -944,10 +982,13 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     if (lane == 0 && rank == 0) {
       const int j = static_cast<int>(warp - kFirstSfWarp);
       uint32_t stage = 0, phase = 0;
-      for (int64_t t = unit0; t < total_units; t += ustride) {
-        const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, 0);
+      for (int64_t t = unit0, u = 0; t < total_units; t += ustride, ++u) {
+        const uint32_t slot = static_cast<uint32_t>(u & 1), ipar = static_cast<uint32_t>((u >> 1) & 1);
+        if (!mbar_wait(info_full_bar(slot), ipar, abort_flag, p.status, p.timeout_ns)) break;
+        const int64_t kb_count = static_cast<int64_t>(info_word[slot] & kInfoKbMask);
+        mbar_arrive(info_empty_bar(slot));
         bool ok = true;
-        for (int64_t kb = 0; kb < ti.kb_count; ++kb) {
+        for (int64_t kb = 0; kb < kb_count; ++kb) {
           // the stage's previous MMAs finished before its producer refilled it
           // (empty barrier), so its scale columns are free once its scale
           // tiles have landed
