@@ -385,6 +385,16 @@ struct StripUnit {
   int g, nt;
 };
 
+// Two fp32 products with one packed multiply (each rounded to nearest even,
+// as two separate multiplies would be).
+__device__ __forceinline__ void fmul2_rn(float a0, float a1, float b, float& p0, float& p1) {
+  uint64_t x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(z));
+}
+
 __global__ void __launch_bounds__(256)
     nvfp4_col_strip_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t cap, int64_t cols,
                            const int64_t* __restrict__ ws, int G, float* __restrict__ outer,
@@ -581,13 +591,18 @@ __global__ void __launch_bounds__(256)
             } else {
               const float ratio = __fdiv_rn(Sv, sbv);
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
+              for (int h = 0; h < 2; ++h) {
+                uint32_t byt[4];  // code pairs in their low bytes
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   const uint32_t w0 = w[16 * bk + 8 * h + 2 * i], w1 = w[16 * bk + 8 * h + 2 * i + 1];
-                  const float v0 = cc ? bf16hi(w0) : bf16lo(w0), v1 = cc ? bf16hi(w1) : bf16lo(w1);
-                  o[2 * bk + h] |= cvt_e2m1x2(__fmul_rn(v0, ratio), __fmul_rn(v1, ratio)) << (8 * i);
+                  float p0, p1;
+                  fmul2_rn(cc ? bf16hi(w0) : bf16lo(w0), cc ? bf16hi(w1) : bf16lo(w1), ratio, p0, p1);
+                  byt[i] = cvt_e2m1x2(p0, p1);
                 }
+                o[2 * bk + h] = __byte_perm(__byte_perm(byt[0], byt[1], 0x0040),
+                                            __byte_perm(byt[2], byt[3], 0x0040), 0x5410);
+              }
             }
             sword |= sbyte << (8 * bk);
           }

@@ -299,3 +299,48 @@ def test_nvfp4_colwise_parity(sizes):
     refr = oracle.nvfp4_quantize(xb, live, R)
     assert np.array_equal(out["q_row"][:live].cpu().numpy(), refr["q_row"][:live])
     assert np.array_equal(out["outer_row"][:live].cpu().numpy(), refr["outer_row"][:live])
+
+
+def test_nvfp4_colwise_special_columns():
+    """Columns at the edges of the scale arithmetic, bit-exact against the
+    oracle: zero and signed-zero columns, a single nonzero, a block far below
+    its column's amax, magnitudes near the bf16 limits (the per-block ratio
+    S / sb then leaves the normal fp32 range and the kernel falls back to the
+    division), and columns scaled by powers of two across the exponent
+    range."""
+    sizes = (256, 128)
+    G, K = len(sizes), 128
+    live = sum(sizes)
+    R = live + 128
+    x = workloads.random_bf16((R, K), seed=95, dist="student_t3").to(torch.float32)
+    x[:, 0] = 0.0
+    x[:, 1] = -0.0
+    x[:, 2] = 0.0
+    x[17, 2] = -3.5                                   # single nonzero: scale 448, code -6
+    x[32:48, 3] = 1e-8                                # a block far below the column amax
+    x[:, 4] = torch.linspace(-1e30, 1e30, R)
+    x[:, 5] = 2.0 ** -133                             # S = 2688 / A overflows to inf
+    x[::2, 6] = 6.0
+    x[1::2, 6] = -0.25
+    x[:, 7] = 3.0e38 * torch.sign(x[:, 7])            # amax near the bf16 maximum
+    x[:, 8] = x[:, 8] * 1e-37                         # tiny, partly subnormal bf16
+    x[300:310, 9] = 3.0e38                            # one huge block in a group of small values
+    x[310:, 9] = x[310:, 9] * 1e-30
+    for c in range(10, K):
+        x[:, c] = x[:, c] * 2.0 ** ((c * 37) % 201 - 100)
+    xb = x.to(torch.bfloat16)
+    assert torch.isfinite(xb).all()
+    ws, st = gpu_offsets(torch.tensor(sizes, dtype=torch.int32), K, R)
+    out = mxg.alloc_nvfp4(R, K, device=DEV, rowwise=False, colwise=True, G=G)
+    for k in ("q_col", "sf_col"):
+        out[k].fill_(0x3C)
+    mxg.mxg_group_quantize(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_COLWISE, xb.to(DEV), R, K, ws, G,
+                           None, None, out["q_col"], out["sf_col"], None, st,
+                           outer_col=out["outer_col"])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    ref = oracle.nvfp4_quantize_colwise(xb, offs, R, fill=0x3C)
+    assert np.array_equal(out["q_col"].cpu().numpy(), ref["q_col"])
+    assert np.array_equal(u8(out["sf_col"]), ref["sf_col"])
+    assert np.array_equal(out["outer_col"].cpu().numpy(), ref["outer_col"])
