@@ -74,8 +74,16 @@ GEMM_SOURCES = ("gemm.cu", "mxg_device.cuh", "mxg_host.h", "tmap.cu")
 # any change to either, "traffic" is reported as null until the counters are
 # taken again.
 GEMM_DRAM_TRAFFIC = {
-    "digest": None,
-    "bytes": {},
+    "digest": "f3a8199d539c11fd13c3a768ed829e320e29f561902e34c1d7f3f3532b4790c3",
+    "bytes": {
+        "mixtral_fprop_mxfp8": 1013425920,
+        "finegrained_fprop_mxfp8": 264913152,
+        "wgrad_mxfp8": 1232272896,
+        "rowscaled_fprop_nvfp4": 341480960,
+        "wgrad_nvfp4": 1064986624,
+        "dgrad_mxfp8": 1392282368,
+        "mixtral_fprop_mxfp8_unaligned": 999685632,
+    },
 }
 
 
