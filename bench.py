@@ -74,7 +74,7 @@ GEMM_SOURCES = ("gemm.cu", "mxg_device.cuh", "mxg_host.h", "tmap.cu")
 # any change to either, "traffic" is reported as null until the counters are
 # taken again.
 GEMM_DRAM_TRAFFIC = {
-    "digest": "f3a8199d539c11fd13c3a768ed829e320e29f561902e34c1d7f3f3532b4790c3",
+    "digest": "f8d2098a5ba4a5a56acf4f7c6318587edd1493c09c0b5bbafc964f431dcdbaeb",
     "bytes": {
         "mixtral_fprop_mxfp8": 1013425920,
         "finegrained_fprop_mxfp8": 264913152,
@@ -106,7 +106,11 @@ def gemm_source_digest() -> str:
     for f in GEMM_SOURCES:
         with open(os.path.join(ROOT, "moe_grouped_block_gb300", "csrc", f)) as fh:
             h.update(code_only(fh.read()).encode())
-    h.update(" ".join(mxg_build.ARCH + mxg_build.NVCC_FLAGS).encode())
+    # include paths relative to the repository, so that a checkout elsewhere
+    # (another machine) gives the same digest
+    flags = [("-I" + os.path.relpath(f[2:], ROOT)) if f.startswith("-I") else f
+             for f in mxg_build.ARCH + mxg_build.NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 

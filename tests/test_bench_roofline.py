@@ -148,3 +148,23 @@ def test_single_core_child_runs_the_same_pass():
     smp = bench.oracle_sample(wl, workloads.make_inputs(wl))
     r = bench.single_core_pass(wl, smp)
     assert r is not None and r[1] == bench.oracle_pass(wl, smp)[1]
+
+
+def test_digest_does_not_depend_on_the_checkout_path(monkeypatch):
+    """The recorded digest must match on another machine, where the repository
+    sits elsewhere and the include flag names that path."""
+    from moe_grouped_block_gb300 import build as mxg_build
+    d0 = bench.gemm_source_digest()
+    moved = [("-I/elsewhere/checkout/include" if f.startswith("-I") else f)
+             for f in mxg_build.NVCC_FLAGS]
+    monkeypatch.setattr(bench, "ROOT", "/elsewhere/checkout")
+    monkeypatch.setattr(mxg_build, "NVCC_FLAGS", moved)
+    src_root = os.path.join(os.path.dirname(os.path.abspath(bench.__file__)))
+    real_open = open
+
+    def open_from_repo(path, *a, **k):
+        if str(path).startswith("/elsewhere/checkout"):
+            path = src_root + str(path)[len("/elsewhere/checkout"):]
+        return real_open(path, *a, **k)
+    monkeypatch.setattr("builtins.open", open_from_repo)
+    assert bench.gemm_source_digest() == d0
