@@ -264,6 +264,14 @@ __device__ __forceinline__ float4 load4(const float* p, bool vec) {
 // bias (bs); column j is lane j / 4's component j % 4, fetched with a
 // shuffle.  (Loading them per 16-column chunk instead put a load latency in
 // front of every chunk: the NVFP4 epilogue took twice as long.)
+__device__ __forceinline__ float4 lds_f4_volatile(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 struct EpiCols {
   float4 cs, bs;
 };
@@ -304,10 +312,14 @@ __device__ __forceinline__ float col_value(const float4& v4, int j) {
 // (NVFP4 column outer scales, bias) come from ec by shuffle, so every lane
 // of the warp runs the transform (rows past row_end only skip the loads and
 // stores); beta and bias checks are made once per row, not per element.
-template <bool NVF4>
+// SMCOLS: the column operands are read from the warp's shared-memory copy
+// (scs: the 128 column outer scales, sbs: the 128 bias values), one
+// broadcast 16-byte load per 4 columns, instead of a shuffle per element.
+template <bool NVF4, bool SMCOLS = false>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
                                              uint32_t col0, uint32_t (&v)[4][32], bool has_k,
-                                             const EpiCols& ec) {
+                                             const EpiCols& ec, const float* scs = nullptr,
+                                             const float* sbs = nullptr) {
   if (ti.c_col + col0 >= p.out_cols) return;  // warp-uniform
   const bool valid = row < ti.row_end;
   const int64_t cbase = row * p.out_cols + ti.c_col + col0;
@@ -315,19 +327,50 @@ __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo
   const float beta = valid && p.beta ? p.beta[ti.g] : 0.0f;  // old C read for valid rows only
   const bool bs = p.bias != nullptr;
   const float rs = NVF4 ? (valid ? p.a_outer[row] : 0.0f) : 1.0f;
+  const float rsa = rs * alpha;  // the row's factor (shared-memory column path)
   // 16 columns at a time (32 bytes of bf16 or 64 of fp32), transformed in
   // place in the accumulator registers
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     uint32_t* a = &v[k >> 1][16 * (k & 1)];
     const int j0 = 16 * k;  // first column of the 16
+    if (SMCOLS) {
+      // pairs of columns: (acc * (alpha * outer_row)) * outer_col [+ bias],
+      // two lanes per packed instruction
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float x = has_k ? __uint_as_float(a[e]) : 0.0f;
-      if (NVF4) x = x * rs * col_value(ec.cs, j0 + e);
-      x *= alpha;
-      if (bs) x += col_value(ec.bs, j0 + e);
-      a[e] = __float_as_uint(x);
+      for (int e = 0; e < 16; e += 4) {
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = has_k ? __uint_as_float(a[e + i]) : 0.0f;
+        f32x2_mul(x[0], x[1], rsa, rsa);
+        f32x2_mul(x[2], x[3], rsa, rsa);
+        // NVFP4: volatile loads, kept next to their use, so the compiler does
+        // not hoist all 128 columns' operands into registers beside the
+        // accumulator (that kernel spilled 104 bytes without them); the MXFP8
+        // kernel has the registers and schedules plain loads better
+        if (NVF4) {
+          const float4 c4 = lds_f4_volatile(smem_u32(scs + j0 + e));
+          f32x2_mul(x[0], x[1], c4.x, c4.y);
+          f32x2_mul(x[2], x[3], c4.z, c4.w);
+        }
+        if (bs) {
+          const float4 b4 = NVF4 ? lds_f4_volatile(smem_u32(sbs + j0 + e))
+                                 : *reinterpret_cast<const float4*>(sbs + j0 + e);
+          f32x2_add(x[0], x[1], b4.x, b4.y);
+          f32x2_add(x[2], x[3], b4.z, b4.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[e + i] = __float_as_uint(x[i]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float x = has_k ? __uint_as_float(a[e]) : 0.0f;
+        if (NVF4) x = x * rs * col_value(ec.cs, j0 + e);
+        x *= alpha;
+        if (bs) x += col_value(ec.bs, j0 + e);
+        a[e] = __float_as_uint(x);
+      }
     }
     if (p.out_bf16) {
       uint16_t* dst = static_cast<uint16_t*>(p.C) + cbase + j0;
@@ -648,8 +691,14 @@ struct PairCfg {
   // full[S], empty[S], sffull[S], tfull, tempty, drain, sfdrain,
   // info_full[2], info_empty[2], two unit words; TMEM base; abort flag
   static constexpr int kBarBytes = 8 * (3 * STAGES + 10) + 16;
-  static size_t smem_bytes(int G) {
-    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16;
+  // column operands staged per epilogue warp (128 floats each): the NVFP4
+  // column outer scales, the bias
+  static size_t col_bytes(bool bias) {
+    return static_cast<size_t>((NVF4 ? 1 : 0) + (bias ? 1 : 0)) * kEpiWarps * 128 * 4;
+  }
+  static size_t smem_bytes(int G, bool bias) {
+    return 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + 12 * (G + 1) + 16 +
+           col_bytes(bias);
   }
   // M = 256 (the pair), N = 256; other fields as in GemmCfg
   static constexpr uint32_t kIdesc = (NVF4 ? ((1u << 7) | (1u << 10)) : 0u) |
@@ -778,6 +827,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
   int32_t* row_off = reinterpret_cast<int32_t*>(bar_area + Cfg::kBarBytes);
   int32_t* tile_off = row_off + (p.G + 1);
   int32_t* prow_off = tile_off + (p.G + 1);
+  // after the tables: the epilogue warps' column operands (NVFP4 column
+  // outer scales, then bias), 128 floats per warp each
+  float* colsm = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(prow_off + (p.G + 1)) + 15) & ~static_cast<uintptr_t>(15));
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
   const uint32_t smem_base = smem_u32(smem);
@@ -1037,7 +1090,32 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
     uint32_t acc_phase = 0;
     for (int64_t t = unit0; t < total_units; t += ustride) {
       const TileInfo ti = map_unit_pair<EPB, BK>(t, p, row_off, prow_off, tile_off, rank);
-      const EpiCols ec = epi_cols<NVF4>(p, ti, col0, lane);  // in flight during the wait
+      // this warp's 128 columns' operands (NVFP4 column outer scales, bias)
+      // copied into its shared-memory slots while it waits (lane l: columns
+      // 4l..4l+3), read back by every lane in the epilogue
+      float* scs = colsm + ew * 128;
+      float* sbs = colsm + ((NVF4 ? Cfg::kEpiWarps : 0) + ew) * 128;
+      __syncwarp();  // the previous unit's reads of the slots are done
+      if ((NVF4 || p.bias) && ti.c_col + col0 < p.out_cols) {
+        const float* srcs[2] = {
+            NVF4 ? p.b_outer + (p.mode == 1 ? static_cast<int64_t>(ti.g) * p.K : 0) + ti.b_row +
+                       col0 + 4 * lane
+                 : nullptr,
+            p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.out_cols + ti.c_col + col0 + 4 * lane
+                   : nullptr};
+        float* dsts[2] = {scs + 4 * lane, sbs + 4 * lane};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          if (!srcs[q]) continue;
+          if (p.vec_col) {
+            cp_async_16(smem_u32(dsts[q]), srcs[q]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) cp_async_4(smem_u32(dsts[q] + c), srcs[q] + c);
+          }
+        }
+      }
+      cp_async_commit();
       if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
       uint32_t v[4][32];
@@ -1055,7 +1133,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty_even);
       acc_phase ^= 1u;
-      epilogue_row<NVF4>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k, ec);
+      cp_async_wait_all();
+      __syncwarp();  // every lane's copies have landed
+      epilogue_row<NVF4, true>(p, ti, ti.c_row + 32 * quarter + lane, col0, v, has_k, EpiCols{},
+                               scs, sbs);
     }
   }
 
@@ -1131,7 +1212,7 @@ cudaError_t launch_pair_variant(const CUtensorMap& ta, const CUtensorMap& tb,
                                 cudaStream_t stream) {
   using Cfg = PairCfg<STAGES, NVF4, BKB>;
   auto kern = grouped_gemm_pair_kernel<STAGES, NVF4, BKB>;
-  const size_t smem = Cfg::smem_bytes(p.G);
+  const size_t smem = Cfg::smem_bytes(p.G, p.bias != nullptr);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
