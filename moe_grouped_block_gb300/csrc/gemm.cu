@@ -1116,7 +1116,10 @@ __global__ void __launch_bounds__(PairCfg<STAGES, NVF4, BKB>::kThreads, 1)
         }
       }
       cp_async_commit();
-      if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, p.timeout_ns)) {
+        cp_async_wait_all();  // no copy into this CTA's shared memory outlives it
+        break;
+      }
       tc_fence_after();
       uint32_t v[4][32];
       const bool has_k = ti.kb_count > 0;
