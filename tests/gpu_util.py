@@ -78,6 +78,41 @@ def normwise_errors(got: np.ndarray, ref: np.ndarray, offs, rows=None):
     return np.array(errs)
 
 
+# Elementwise relative error is taken over the elements with |ref| >= 1e-2 of
+# their expert's max|ref| (near-cancelling elements have no meaningful
+# relative error); it is reported beside the normwise gate, with a loose
+# sanity bound.
+ELEM_FLOOR = 1e-2
+ELEM_BOUND = 1e-2
+
+
+def elementwise_error(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got-ref| / |ref| over the elements of one expert block with
+    |ref| >= ELEM_FLOOR * max|ref|."""
+    den = np.max(np.abs(ref)) if ref.size else 0.0
+    if den == 0:
+        return 0.0
+    sel = np.abs(ref) >= ELEM_FLOOR * den
+    return float(np.max(np.abs(got[sel] - ref[sel]) / np.abs(ref[sel])))
+
+
+def elementwise_errors(got: np.ndarray, ref: np.ndarray, offs, rows=None):
+    """elementwise_error per expert (rows grouped as in normwise_errors)."""
+    rows = np.arange(got.shape[0]) if rows is None else np.asarray(rows)
+    errs = []
+    for g in range(len(offs) - 1):
+        sel = (rows >= offs[g]) & (rows < offs[g + 1])
+        if sel.any():
+            errs.append(elementwise_error(got[sel], ref[sel]))
+    return np.array(errs)
+
+
+def report_errors(name: str, normwise, elementwise) -> None:
+    """One line per full-size check (shown with pytest -rP)."""
+    print("%s: normwise max %.3e, elementwise max over |R| >= %.0e max|R|: %.3e"
+          % (name, float(np.max(normwise)), ELEM_FLOOR, float(np.max(elementwise))))
+
+
 class gemm_override:
     """Context manager that routes mxg.mxg_grouped_gemm through the test entry
     point mxg_grouped_gemm_debug with a forced kernel choice: tile_n = 256 or
