@@ -258,12 +258,8 @@ __device__ __forceinline__ float4 load4(const float* p, bool vec) {
   return make_float4(p[0], p[1], p[2], p[3]);
 }
 
-// Column operands of an epilogue warp's 128 columns, read once per unit
-// before the accumulator is (in flight while the warp waits for it): lane l
-// holds columns 4l .. 4l+3 of the NVFP4 column outer scales (cs) and of the
-// bias (bs); column j is lane j / 4's component j % 4, fetched with a
-// shuffle.  (Loading them per 16-column chunk instead put a load latency in
-// front of every chunk: the NVFP4 epilogue took twice as long.)
+// A 16-byte shared-memory load the compiler keeps where it is written
+// (neither hoisted nor merged with its neighbours).
 __device__ __forceinline__ float4 lds_f4_volatile(uint32_t addr) {
   float4 v;
   asm volatile("ld.volatile.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -272,6 +268,13 @@ __device__ __forceinline__ float4 lds_f4_volatile(uint32_t addr) {
   return v;
 }
 
+// Column operands of an epilogue warp's 128 columns in the single-CTA
+// kernel, read once per unit before the accumulator is (in flight while the
+// warp waits for it): lane l holds columns 4l .. 4l+3 of the NVFP4 column
+// outer scales (cs) and of the bias (bs); column j is lane j / 4's component
+// j % 4, fetched with a shuffle.  (Loading them per 16-column chunk instead
+// put a load latency in front of every chunk: the NVFP4 epilogue took twice
+// as long.)  The CTA-pair kernel copies them to shared memory instead.
 struct EpiCols {
   float4 cs, bs;
 };
@@ -309,12 +312,12 @@ __device__ __forceinline__ float col_value(const float4& v4, int j) {
 // skipped.  Each thread owns a row, so a store instruction touches 32 rows:
 // with a 32-byte-aligned C every store fills whole 32-byte sectors (16 bf16
 // or 8 fp32 per store), else 16-byte stores are used.  The column operands
-// (NVFP4 column outer scales, bias) come from ec by shuffle, so every lane
-// of the warp runs the transform (rows past row_end only skip the loads and
-// stores); beta and bias checks are made once per row, not per element.
-// SMCOLS: the column operands are read from the warp's shared-memory copy
-// (scs: the 128 column outer scales, sbs: the 128 bias values), one
-// broadcast 16-byte load per 4 columns, instead of a shuffle per element.
+// (NVFP4 column outer scales, bias) come from ec by shuffle, or with SMCOLS
+// from the warp's shared-memory copy (scs: the 128 column outer scales, sbs:
+// the 128 bias values), one broadcast 16-byte load per 4 columns; either way
+// every lane of the warp runs the transform (rows past row_end only skip the
+// loads and stores); beta and bias checks are made once per row, not per
+// element.
 template <bool NVF4, bool SMCOLS = false>
 __device__ __forceinline__ void epilogue_row(const GemmParams& p, const TileInfo& ti, int64_t row,
                                              uint32_t col0, uint32_t (&v)[4][32], bool has_k,
