@@ -22,9 +22,14 @@
 //     units with the cta_group::2 MMA (each CTA holds 128 rows of A and half
 //     of B); warp 0 lane 0 TMA producer, warp 1 lane 0 MMA issuer (even CTA),
 //     warps 2-9 epilogue (one TMEM lane quarter and 128 columns each), warps
-//     10-11 scale copies (even CTA).  128 bytes of K per pipeline stage (4
-//     MMAs of 32 bytes: 32 E4M3 or 64 E2M1 elements), 256 bytes for MXFP8
-//     fprop when K % 256 == 0, 64 for NVFP4 where 256 elements do not fit.
+//     10-11 scale copies (even CTA).  The producer publishes each unit's
+//     shape (K blocks, MMAs of the last one, half width) to the MMA thread
+//     and the copy warps, so that they decode nothing between units.  128
+//     bytes of K per pipeline stage (4 MMAs of 32 bytes: 32 E4M3 or 64 E2M1
+//     elements), 256 bytes for MXFP8 fprop when K % 256 == 0 and for MXFP8
+//     wgrad (a group may end inside its last stage), 64 for NVFP4 fprop with
+//     K % 256 != 0.  The epilogue warps copy their columns' operands (NVFP4
+//     column outer scales, bias) into shared memory while they wait.
 //   * grouped_gemm_kernel: single-CTA 128 x BN tiles (BN 256 or 128) for the
 //     cases the pair does not cover (B with fewer than 256 rows); warps
 //     0 / 1 / 2.. as above, scale copies inline on the MMA thread.
