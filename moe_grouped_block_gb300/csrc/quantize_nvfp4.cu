@@ -17,11 +17,12 @@
 // each run of 4 scale bytes, contiguous in the swizzled layout, as one 32-bit
 // store); wider rows take one warp per row that reads the row twice from
 // global memory.
-// Colwise (the wgrad operands, per-(group, column) outer scale): zero the
-// [G, cols] outer buffer; an amax pass over 128 x 128 TMA-staged tiles folds
-// column maxima into it with atomicMax; a quantize pass walks the tiles in
-// reverse order (starting on the tiles still in L2) and writes the transposed
-// codes and swizzled scales; a last launch turns the amax into A / 2688.
+// Colwise (the wgrad operands, per-(group, column) outer scale), one launch:
+// a CTA owns one group's rows in a 64-column strip; an amax pass streams the
+// strip's 256 x 64 TMA tiles and writes the strip's outer scales A / 2688, a
+// quantize pass streams them again in reverse order (starting on the tiles
+// still in L2) and writes the transposed codes and swizzled scales.
+// Products are packed fp32x2 multiplies; four E2M1 conversions fill a word.
 #include <algorithm>
 
 #include "mxg_device.cuh"
