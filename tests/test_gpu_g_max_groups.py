@@ -47,6 +47,27 @@ def test_fprop_max_groups(K):
     assert errs.max() <= TOL, errs
 
 
+@pytest.mark.parametrize("fmt,K", [("mxfp8", 256), ("mxfp8", 384), ("nvfp4", 256),
+                                   ("nvfp4", 384)])
+def test_fprop_max_groups_bias(fmt, K):
+    # The CTA-pair kernel's largest shared-memory layouts: 1024 groups' tables
+    # beside every epilogue warp's staged bias (and, NVFP4, column outer
+    # scales), on each stage variant (MXFP8 3 x 256 / 6 x 128 bytes of K,
+    # NVFP4 5 x 128 / 10 x 64).
+    base = "mixtral_fprop_mxfp8" if fmt == "mxfp8" else "rowscaled_fprop_nvfp4"
+    wl = workloads.WORKLOADS[base].scaled(
+        G=G, M=4096, K=K, N=256, sizes="fixed", fixed_sizes=_aligned_sizes(4096, 20, 93))
+    rng = np.random.default_rng(94)
+    bias = rng.standard_normal((G, wl.N)).astype(np.float32)
+    alpha = (0.5 + rng.random(G)).astype(np.float32).tolist()
+    case = fprop_case(wl, fill_c=7.0, bias=bias, alpha=alpha)
+    assert int(case["status"].item()) == 0
+    offs, rows, cols, ref, a, b = oracle_fprop(wl, case["inp"], alpha=alpha, bias=bias)
+    got = case["C"].cpu().numpy().astype(np.float64)
+    errs = normwise_errors(got[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
 def test_wgrad_max_groups():
     wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(
         G=G, M=4096, K=256, N=128, sizes="fixed", fixed_sizes=_aligned_sizes(4096, 24, 92))
