@@ -295,6 +295,30 @@ def test_stage_width_fprop_and_dgrad(N, bk):
     _dgrad_check(None, 512, N)
 
 
+@pytest.mark.parametrize("tn", [None, 128])
+def test_fprop_one_k_block(tn):
+    # K = 128: every unit is one 128-byte K stage (the 256-byte stages need
+    # K % 256 == 0), so the first K block is also the last
+    wl = workloads.WORKLOADS["mixtral_fprop_mxfp8"].scaled(M=1024, K=128, N=512)
+    case, offs, rows, ref = _run_fprop(wl, tn)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+def test_nvfp4_fprop_one_k_block():
+    # K = 128: one 64-byte stage (two MMAs) per unit
+    wl = workloads.WORKLOADS["rowscaled_fprop_nvfp4"].scaled(M=1024, K=128, N=512, G=4)
+    case, offs, rows, ref = _run_fprop(wl)
+    errs = normwise_errors(case["C"].cpu().numpy().astype(np.float64)[:wl.M], ref, offs)
+    assert errs.max() <= TOL, errs
+
+
+@pytest.mark.parametrize("tn", [None, 128])
+def test_dgrad_one_k_block(tn):
+    """dgrad contracting over N = 128: one 128-byte K block per unit."""
+    _dgrad_check(tn, 256, 128)
+
+
 def _dgrad_check(tn, K, N):
     wl = workloads.WORKLOADS["finegrained_fprop_mxfp8"].scaled(M=2048, K=K, N=N, G=8)
     inp = workloads.make_inputs(wl)
@@ -329,11 +353,15 @@ def _dgrad_check(tn, K, N):
 
 
 # --------------------------------------------------------------------------- NVFP4 wgrad
-@pytest.mark.parametrize("K", [512, 384])
-def test_nvfp4_wgrad_scaled(K):
+@pytest.mark.parametrize("K,sizes", [(512, None), (384, None),
+                                     (256, (128, 384, 0, 128, 640, 256, 128, 384))])
+def test_nvfp4_wgrad_scaled(K, sizes):
     """Row-scaled NVFP4 wgrad: colwise copies with per-(group, column) outer
-    scales (PR #3661's wgrad direction)."""
+    scales (PR #3661's wgrad direction).  The fixed sizes end groups inside a
+    256-element K stage (128 and 384 rows) and leave one group empty."""
     wl = workloads.WORKLOADS["wgrad_mxfp8"].scaled(M=2048, K=K, N=256)
+    if sizes is not None:
+        wl = wl.scaled(sizes="fixed", fixed_sizes=sizes)
     inp = workloads.make_inputs(wl)
     G, N, M = wl.G, wl.N, wl.M
     sizes = inp["sizes"].numpy()
