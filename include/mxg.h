@@ -214,7 +214,9 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *   B = colwise copy of X:  data [K, M_cap], scale [K, M_cap/32].
  *   dW[g, n, k] = alpha_g * sum_{m in group g} A[n, m] * B[k, m]
  *                 + beta_g * dW[g, n, k];   C = dW is [G, N, K].
- *   An empty group writes beta_g * dW[g] (zeros when beta is NULL).
+ *   An empty group writes beta_g * dW[g] (zeros when beta is NULL or
+ *   beta_g is 0).  With M_cap = 0 every group is empty and A and B are not
+ *   read (their pointers must still be non-NULL).
  * MXG_DGRAD_NN (ragged rows, weights not transposed, MXFP8; [TE-gemm]
  * _quantize_gemm_operands: an RHS whose contraction dim is not last is
  * quantized colwise):
@@ -223,6 +225,7 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
  *       [K, G*N/32] (mxg_group_quantize(MXFP8, COLWISE, W, G*N, K, NULL, ...)).
  *   dX[off_g + i, k] = alpha_g * sum_n A[off_g+i, n] * B[k, g*N + n]
  *                      + beta_g * dX[off_g + i, k];   C = dX is [M_cap, K].
+ * M_cap = 0: fprop and dgrad have no output rows and launch nothing.
  * group_ws : offsets workspace of mxg_group_offsets (first G entries used).
  * alpha, beta : device float[G] or NULL (alpha = 1, beta = 0).
  * bias  : device float [G, N] (fprop) or [G, K] (dgrad), or NULL: per-group

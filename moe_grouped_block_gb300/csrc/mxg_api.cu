@@ -32,6 +32,8 @@ cudaError_t launch_grouped_gemm(bool nvfp4, int mode, const void* a_data, const 
                                 int num_sms, int tile_n, int stage_bytes, int inject,
                                 uint64_t timeout_ns, int unaligned, int64_t a_ld_bytes,
                                 int64_t b_ld_bytes, cudaStream_t stream);
+cudaError_t launch_wgrad_no_rows(int G, int64_t N, int64_t K, const float* beta, void* C,
+                                 int out_bf16, int num_sms, cudaStream_t stream);
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 }  // namespace mxg
 
@@ -275,7 +277,14 @@ static mxg_status_t grouped_gemm_impl(mxg_format_t fmt, mxg_gemm_mode_t mode,
   int sms = 0;
   const mxg_status_t st = current_device(&sms);
   if (st != MXG_OK) return st;
-  if (M_cap == 0) return MXG_OK;
+  if (M_cap == 0) {
+    // no rows: the fprop and dgrad outputs are empty; every wgrad group is
+    // empty, and each dW_g is written as for an empty group
+    if (mode != MXG_WGRAD_NT) return MXG_OK;
+    return launched(mxg::launch_wgrad_no_rows(G, N, K, beta, C, out_type == MXG_OUT_BF16 ? 1 : 0,
+                                              sms, reinterpret_cast<cudaStream_t>(stream)),
+                    1);
+  }
   return launched(mxg::launch_grouped_gemm(
                       nv, mode == MXG_WGRAD_NT ? 1 : (mode == MXG_DGRAD_NN ? 2 : 0), A->data, A->scale, A->outer, B->data,
                       B->scale, B->outer, group_ws, G, M_cap, N, K, alpha, beta, bias, C,

@@ -15,7 +15,7 @@ import oracle
 from moe_grouped_block_gb300 import mxg, workloads
 
 from gpu_util import (DEV, fprop_case, gpu_mxfp8, gpu_offsets, normwise_errors, oracle_fprop,
-                      oracle_quantized_operands, require_gpu, tile_n, u8,
+                      oracle_quantized_operands, require_gpu, status_tensor, tile_n, u8,
                       gemm_override)
 
 pytestmark = pytest.mark.gpu
@@ -394,6 +394,56 @@ def test_nvfp4_wgrad_scaled(K, sizes):
             assert not got[g].any()
         else:
             assert np.abs(got[g] - ref[g]).max() / np.abs(ref[g]).max() <= TOL, g
+
+
+@pytest.mark.parametrize("entry", ["aligned", "unaligned", "nvfp4"])
+@pytest.mark.parametrize("out_type", [mxg.MXG_OUT_F32, mxg.MXG_OUT_BF16])
+def test_wgrad_without_rows(entry, out_type):
+    """M_cap = 0: every group is empty, so each dW_g is beta_g * dW_g, or 0
+    where there is no beta or beta_g is 0 (the oracle's empty group); the
+    operands have no columns and are not read.  fprop and dgrad with
+    M_cap = 0 write nothing."""
+    G, N, K = 4, 256, 384
+    zero = torch.zeros(G, dtype=torch.int32)
+    ws = mxg.alloc_offsets(G, DEV)
+    st = status_tensor()
+    if entry == "unaligned":
+        mxg.mxg_group_offsets_unaligned(zero.to(DEV), 1, K, 0, ws, st)
+    else:
+        mxg.mxg_group_offsets(zero.to(DEV), 1, K, 0, ws, st)
+    dummy = torch.zeros(64, dtype=torch.uint8, device=DEV)  # valid pointers, never read
+    outer = torch.zeros(64, dtype=torch.float32, device=DEV)
+    cdt = torch.float32 if out_type == mxg.MXG_OUT_F32 else torch.bfloat16
+    old = workloads.random_bf16((G, N, K), seed=44).float().to(cdt)
+    for beta in ([0.5, 0.0, -2.0, 1.0], None):
+        if entry == "nvfp4" and beta is not None:
+            continue  # beta is rejected with NVFP4
+        dW = old.to(DEV).clone()
+        be = None if beta is None else torch.tensor(beta, dtype=torch.float32, device=DEV)
+        if entry == "unaligned":
+            mxg.mxg_grouped_gemm_unaligned(mxg.MXG_WGRAD_NT, (dummy, dummy), (dummy, dummy), ws, G,
+                                           0, N, K, None, be, dW, out_type, dev_status=st)
+        elif entry == "nvfp4":
+            mxg.mxg_grouped_gemm(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_WGRAD_NT, (dummy, dummy, outer),
+                                 (dummy, dummy, outer), ws, G, 0, N, K, None, None, dW, out_type,
+                                 dev_status=st)
+        else:
+            mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mxg.MXG_WGRAD_NT, (dummy, dummy, None),
+                                 (dummy, dummy, None), ws, G, 0, N, K, None, be, dW, out_type,
+                                 dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        b = torch.zeros(G) if beta is None else torch.tensor(beta)
+        want = (old.float() * b.view(G, 1, 1)).to(cdt)  # one rounding, as the epilogue's
+        want[b == 0] = 0
+        assert torch.equal(dW.cpu(), want), beta
+    if entry == "aligned":
+        C = torch.full((128, N), 5.0, dtype=torch.float32, device=DEV)
+        for mode, n_ in ((mxg.MXG_FPROP_TN, N), (mxg.MXG_DGRAD_NN, N)):
+            mxg.mxg_grouped_gemm(mxg.MXG_MXFP8_E4M3, mode, (dummy, dummy, None),
+                                 (dummy, dummy, None), ws, G, 0, n_, K, C=C, dev_status=st)
+        torch.cuda.synchronize()
+        assert torch.all(C == 5.0)
 
 
 @pytest.mark.parametrize("tn", [None, 128])
