@@ -207,8 +207,18 @@ mxg_status_t mxg_group_quantize(mxg_format_t fmt, mxg_qlayout_t layout, const vo
   int sms = 0;
   const mxg_status_t st = current_device(&sms);
   if (st != MXG_OK) return st;
-  if (rows_capacity == 0) return MXG_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (rows_capacity == 0) {
+    // no rows: every group is empty, and the NVFP4 colwise outer scales of an
+    // empty group are 0 (the colwise kernel needs rows for its tensor map)
+    if (fmt == MXG_NVFP4_ROWSCALED && col &&
+        cudaMemsetAsync(outer_col, 0,
+                        static_cast<size_t>(group_ws ? G : 1) * static_cast<size_t>(cols) *
+                            sizeof(float),
+                        s) != cudaSuccess)
+      return MXG_ERR_LAUNCH;
+    return MXG_OK;
+  }
   if (fmt == MXG_MXFP8_E4M3)
     return launched(mxg::launch_mxfp8_quantize(row, col, static_cast<const uint16_t*>(x),
                                                rows_capacity, cols, group_ws, G,

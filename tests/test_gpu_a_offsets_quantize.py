@@ -301,6 +301,25 @@ def test_nvfp4_colwise_parity(sizes):
     assert np.array_equal(out["outer_row"][:live].cpu().numpy(), refr["outer_row"][:live])
 
 
+def test_quantize_without_rows():
+    """rows_capacity = 0: no rows are read or written; the NVFP4 colwise outer
+    scales, one per (group, column), are those of empty groups: 0."""
+    G, cols = 3, 256
+    zero = torch.zeros(G, dtype=torch.int32)
+    ws, st = gpu_offsets(zero, cols, 0)
+    x = torch.zeros(64, dtype=torch.bfloat16, device=DEV)  # valid pointers, never touched
+    dummy = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    outer = torch.full((G, cols), 7.0, dtype=torch.float32, device=DEV)
+    mxg.mxg_group_quantize(mxg.MXG_NVFP4_ROWSCALED, mxg.MXG_COLWISE, x, 0, cols, ws, G, None,
+                           None, dummy, dummy, None, st, outer_col=outer)
+    mxg.mxg_group_quantize(mxg.MXG_MXFP8_E4M3, mxg.MXG_BOTH, x, 0, cols, ws, G, dummy, dummy,
+                           dummy, dummy, None, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.all(outer == 0.0)
+    assert torch.all(dummy == 0)
+
+
 def test_nvfp4_colwise_special_columns():
     """Columns at the edges of the scale arithmetic, bit-exact against the
     oracle: zero and signed-zero columns, a single nonzero, a block far below
